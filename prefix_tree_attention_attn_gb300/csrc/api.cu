@@ -1,0 +1,393 @@
+// C ABI of libtreeattn (see include/tree_attn.h): argument checks, the plan's
+// device copy, TMA tensor maps, and kernel launches.  No CPU fallback exists:
+// without a usable device every compute call returns an error.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "kernels.h"
+#include "plan.h"
+
+namespace treeattn {
+
+// Device status word written by the kernels' bounded waits (0 = fine).
+__device__ int g_device_status = 0;
+
+namespace {
+
+constexpr int kBlock = 128;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---- driver entry point for tensor-map encoding (no link-time libcuda) ------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// [rows, heads, d] bf16, boxes of 64 (d) x 1 (head) x 128 (rows), 128-byte swizzle.
+int make_tmap(CUtensorMap* m, const void* base, int64_t rows, int heads, int d) {
+    EncodeTiledFn enc = get_encode();
+    if (!enc) return TREE_ATTN_ERR_CUDA;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
+    cuuint32_t box[3] = {64, 1, kBlock};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
+}
+
+int current_device(int* dev) {
+    if (cudaGetDevice(dev) != cudaSuccess) return TREE_ATTN_ERR_NO_DEVICE;
+    if (*dev < 0 || *dev >= kMaxDevices) return TREE_ATTN_ERR_NO_DEVICE;
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *dev);
+    if (major != 10 || minor != 3) return TREE_ATTN_ERR_NO_DEVICE;
+    return TREE_ATTN_OK;
+}
+
+// Upload (once per device) the tables the kernels read.
+int ensure_device(tree_attn_plan_s* P, DevicePlan** out) {
+    int dev;
+    int st = current_device(&dev);
+    if (st) return st;
+    std::lock_guard<std::mutex> lk(P->mu);
+    DevicePlan& D = P->dev[dev];
+    if (D.ready) {
+        *out = &D;
+        return TREE_ATTN_OK;
+    }
+    const int64_t T = P->T;
+    const int64_t n_ent = (int64_t)P->qt_kv.size();
+    const int64_t n_items = (int64_t)P->bwd_items.size() / 4;
+    const int64_t n_splits = (int64_t)P->splits.size() / 4;
+    // one int32 buffer: subend | qt_ptr | qt_ent | fwd_order | kv_minsub | items | splits
+    const int64_t sizes[7] = {T * kBlock, T + 1, n_ent, T, T, 4 * n_items, 4 * std::max<int64_t>(n_splits, 1)};
+    int64_t offs[7], total = 0;
+    for (int k = 0; k < 7; ++k) {
+        offs[k] = total;
+        total += (sizes[k] + 63) / 64 * 64;   // 256-byte aligned sections
+    }
+    std::vector<int32_t> h(total, 0);
+    std::copy(P->subend.begin(), P->subend.end(), h.begin() + offs[0]);
+    std::copy(P->qt_ptr.begin(), P->qt_ptr.end(), h.begin() + offs[1]);
+    for (int64_t e = 0; e < n_ent; ++e) {
+        const int32_t c = P->qt_kv[e];
+        // a kv-tile reaching past N is masked per element whatever its class
+        const bool tail = (int64_t)(c + 1) * kBlock > P->N;
+        const bool partial = P->qt_cls[e] == TREE_ATTN_TILE_PARTIAL || tail;
+        h[offs[2] + e] = c * 2 + (partial ? 1 : 0);
+    }
+    std::copy(P->fwd_order.begin(), P->fwd_order.end(), h.begin() + offs[3]);
+    std::copy(P->kv_minsub.begin(), P->kv_minsub.end(), h.begin() + offs[4]);
+    std::copy(P->bwd_items.begin(), P->bwd_items.end(), h.begin() + offs[5]);
+    std::copy(P->splits.begin(), P->splits.end(), h.begin() + offs[6]);
+    void* buf = nullptr;
+    if (cudaMalloc(&buf, total * sizeof(int32_t)) != cudaSuccess) {
+        cudaGetLastError();
+        return TREE_ATTN_ERR_OUT_OF_MEMORY;
+    }
+    if (cudaMemcpy(buf, h.data(), total * sizeof(int32_t), cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaFree(buf);
+        return TREE_ATTN_ERR_CUDA;
+    }
+    int32_t* b = static_cast<int32_t*>(buf);
+    D.base = buf;
+    D.subend = b + offs[0];
+    D.qt_ptr = b + offs[1];
+    D.qt_ent = b + offs[2];
+    D.fwd_order = b + offs[3];
+    D.kv_minsub = b + offs[4];
+    D.bwd_items = b + offs[5];
+    D.splits = b + offs[6];
+    D.ready = true;
+    *out = &D;
+    return TREE_ATTN_OK;
+}
+
+// Address of the status word on the current device (looked up once per device).
+int status_ptr(int dev, int** out) {
+    static int* ptrs[kMaxDevices] = {};
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!ptrs[dev]) {
+        void* a = nullptr;
+        if (cudaGetSymbolAddress(&a, g_device_status) != cudaSuccess) return TREE_ATTN_ERR_CUDA;
+        ptrs[dev] = static_cast<int*>(a);
+    }
+    *out = ptrs[dev];
+    return TREE_ATTN_OK;
+}
+
+int check_heads(const tree_attn_plan_s* P, int hq, int hkv, int d) {
+    if (hq <= 0 || hkv <= 0 || hq % hkv != 0) return TREE_ATTN_ERR_UNSUPPORTED;
+    if (d != 64 && d != 128) return TREE_ATTN_ERR_UNSUPPORTED;
+    if (P->block != kBlock) return TREE_ATTN_ERR_UNSUPPORTED;
+    if ((int64_t)P->N * hq * d > ((int64_t)1 << 40)) return TREE_ATTN_ERR_TOO_LARGE;
+    // grid dimension limit of the forward launch
+    if ((int64_t)P->T * hq > INT32_MAX) return TREE_ATTN_ERR_TOO_LARGE;
+    return TREE_ATTN_OK;
+}
+
+struct WsLayout {
+    size_t dq_acc, delta, lse2, part, total;
+};
+
+WsLayout bwd_layout(const tree_attn_plan_s* P, int hq, int hkv, int d) {
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    const size_t Npad = (size_t)P->T * kBlock;
+    WsLayout w;
+    w.dq_acc = 0;
+    w.delta = w.dq_acc + up((size_t)P->N * hq * d * 4);
+    w.lse2 = w.delta + up(Npad * hq * 4);
+    w.part = w.lse2 + up(Npad * hq * 4);
+    w.total = w.part + up((size_t)P->n_slots * hkv * 2 * kBlock * d * 4);
+    return w;
+}
+
+}  // namespace
+}  // namespace treeattn
+
+using namespace treeattn;
+
+extern "C" {
+
+int tree_attn_plan(const int32_t* parent, const int32_t* seg_len, int32_t n_nodes, const tree_attn_plan_opts_t* opts,
+                   tree_attn_plan_t* out) {
+    if (!out) return TREE_ATTN_ERR_INVALID_ARG;
+    *out = nullptr;
+    tree_attn_plan_s* P = nullptr;
+    int st = build_plan(parent, seg_len, n_nodes, opts, &P);
+    if (st) return st;
+    *out = P;
+    return TREE_ATTN_OK;
+}
+
+int tree_attn_plan_info(tree_attn_plan_t P, tree_attn_plan_info_t* info) {
+    if (!P || !info) return TREE_ATTN_ERR_INVALID_ARG;
+    info->n_tokens = P->N;
+    info->n_nodes = P->n_nodes;
+    info->block = P->block;
+    info->n_qtiles = P->T;
+    info->n_bwd_items = (int32_t)(P->bwd_items.size() / 4);
+    info->n_pairs = P->pairs;
+    info->n_intervals = (int64_t)P->qi_lo.size();
+    info->n_tile_entries = (int64_t)P->qt_kv.size();
+    info->n_full_tiles = P->n_full;
+    info->n_split_kv_tiles = (int32_t)(P->splits.size() / 4);
+    info->bwd_chunk_qtiles = P->chunk;
+    info->n_partial_slots = P->n_slots;
+    return TREE_ATTN_OK;
+}
+
+int tree_attn_plan_export(tree_attn_plan_t P, const tree_attn_plan_arrays_t* d) {
+    if (!P || !d) return TREE_ATTN_ERR_INVALID_ARG;
+    auto cp = [](int32_t* dst, const std::vector<int32_t>& v) {
+        if (dst && !v.empty()) std::memcpy(dst, v.data(), v.size() * sizeof(int32_t));
+    };
+    cp(d->node_order, P->node_order);
+    cp(d->node_off, P->node_off);
+    cp(d->subend, P->subend);
+    cp(d->qi_ptr, P->qi_ptr);
+    cp(d->qi_lo, P->qi_lo);
+    cp(d->qi_hi, P->qi_hi);
+    cp(d->qt_ptr, P->qt_ptr);
+    cp(d->qt_kv, P->qt_kv);
+    if (d->qt_cls && !P->qt_cls.empty()) std::memcpy(d->qt_cls, P->qt_cls.data(), P->qt_cls.size());
+    cp(d->kv_qlo, P->kv_qlo);
+    cp(d->kv_qhi, P->kv_qhi);
+    cp(d->fwd_order, P->fwd_order);
+    cp(d->bwd_items, P->bwd_items);
+    return TREE_ATTN_OK;
+}
+
+int tree_attn_plan_upload(tree_attn_plan_t P) {
+    if (!P) return TREE_ATTN_ERR_INVALID_ARG;
+    DevicePlan* D = nullptr;
+    return ensure_device(P, &D);
+}
+
+int tree_attn_workspace_size(tree_attn_plan_t P, int32_t hq, int32_t hkv, int32_t d, size_t* fwd_bytes,
+                             size_t* bwd_bytes) {
+    if (!P) return TREE_ATTN_ERR_INVALID_ARG;
+    int st = check_heads(P, hq, hkv, d);
+    if (st) return st;
+    if (fwd_bytes) *fwd_bytes = 0;
+    if (bwd_bytes) *bwd_bytes = bwd_layout(P, hq, hkv, d).total;
+    return TREE_ATTN_OK;
+}
+
+int tree_attn_fwd(tree_attn_plan_t P, const void* q, const void* k, const void* v, void* o, float* lse, int32_t hq,
+                  int32_t hkv, int32_t d, float softmax_scale, void* workspace, size_t ws_bytes, void* stream) {
+    (void)workspace;
+    (void)ws_bytes;
+    if (!P || !q || !k || !v || !o || !lse) return TREE_ATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(softmax_scale)) return TREE_ATTN_ERR_INVALID_ARG;
+    int st = check_heads(P, hq, hkv, d);
+    if (st) return st;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return TREE_ATTN_ERR_ALIGNMENT;
+    DevicePlan* D = nullptr;
+    st = ensure_device(P, &D);
+    if (st) return st;
+    CUtensorMap tq, tk, tv, to;
+    if ((st = make_tmap(&tq, q, P->N, hq, d)) || (st = make_tmap(&tk, k, P->N, hkv, d)) ||
+        (st = make_tmap(&tv, v, P->N, hkv, d)) || (st = make_tmap(&to, o, P->N, hq, d)))
+        return st;
+    const int group = hq / hkv;
+    const int ns = (group % 2 == 0) ? 2 : 1;
+    FwdParams p;
+    p.qt_ptr = D->qt_ptr;
+    p.qt_ent = D->qt_ent;
+    p.fwd_order = D->fwd_order;
+    p.subend = D->subend;
+    p.lse = lse;
+    p.N = (int32_t)P->N;
+    p.hq = hq;
+    p.group = group;
+    p.scale_log2 = softmax_scale * 1.4426950408889634f;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if ((st = status_ptr(dev, &p.status))) return st;
+    const int grid = P->T * (hq / ns);
+    cudaError_t e = launch_fwd(d, ns, &tq, &tk, &tv, &to, p, grid, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
+}
+
+int tree_attn_bwd(tree_attn_plan_t P, const void* q, const void* k, const void* v, const void* o, const float* lse,
+                  const void* dout, void* dq, void* dk, void* dv, int32_t hq, int32_t hkv, int32_t d,
+                  float softmax_scale, void* workspace, size_t ws_bytes, void* stream) {
+    if (!P || !q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return TREE_ATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(softmax_scale)) return TREE_ATTN_ERR_INVALID_ARG;
+    int st = check_heads(P, hq, hkv, d);
+    if (st) return st;
+    for (const void* ptr : {q, k, v, o, (const void*)lse, dout, (const void*)dq, (const void*)dk, (const void*)dv})
+        if (!aligned16(ptr)) return TREE_ATTN_ERR_ALIGNMENT;
+    const WsLayout w = bwd_layout(P, hq, hkv, d);
+    if (!workspace || ws_bytes < w.total) return TREE_ATTN_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return TREE_ATTN_ERR_ALIGNMENT;
+    DevicePlan* D = nullptr;
+    st = ensure_device(P, &D);
+    if (st) return st;
+    CUtensorMap tq, tk, tv, tdo;
+    if ((st = make_tmap(&tq, q, P->N, hq, d)) || (st = make_tmap(&tk, k, P->N, hkv, d)) ||
+        (st = make_tmap(&tv, v, P->N, hkv, d)) || (st = make_tmap(&tdo, dout, P->N, hq, d)))
+        return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* ws = static_cast<char*>(workspace);
+    const int32_t Npad = P->T * kBlock;
+
+    BwdPreParams pre;
+    pre.o = static_cast<const uint16_t*>(o);
+    pre.dout = static_cast<const uint16_t*>(dout);
+    pre.lse = lse;
+    pre.delta = reinterpret_cast<float*>(ws + w.delta);
+    pre.lse2 = reinterpret_cast<float*>(ws + w.lse2);
+    pre.dq_acc = reinterpret_cast<float*>(ws + w.dq_acc);
+    pre.N = (int32_t)P->N;
+    pre.Npad = Npad;
+    pre.hq = hq;
+    pre.d = d;
+    cudaError_t e = launch_bwd_pre(pre, s);
+    if (e != cudaSuccess) return TREE_ATTN_ERR_CUDA;
+
+    BwdParams p;
+    p.items = D->bwd_items;
+    p.subend = D->subend;
+    p.kv_minsub = D->kv_minsub;
+    p.delta = pre.delta;
+    p.lse2 = pre.lse2;
+    p.dq_acc = pre.dq_acc;
+    p.dk = static_cast<uint16_t*>(dk);
+    p.dv = static_cast<uint16_t*>(dv);
+    p.part = reinterpret_cast<float*>(ws + w.part);
+    p.N = (int32_t)P->N;
+    p.Npad = Npad;
+    p.hq = hq;
+    p.hkv = hkv;
+    p.group = hq / hkv;
+    p.scale = softmax_scale;
+    p.scale_log2 = softmax_scale * 1.4426950408889634f;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if ((st = status_ptr(dev, &p.status))) return st;
+    const int64_t n_items = (int64_t)P->bwd_items.size() / 4;
+    if (n_items * hkv > INT32_MAX) return TREE_ATTN_ERR_TOO_LARGE;
+    e = launch_bwd(d, &tq, &tk, &tv, &tdo, p, (int)(n_items * hkv), s);
+    if (e != cudaSuccess) return TREE_ATTN_ERR_CUDA;
+
+    BwdPostParams post;
+    post.dq_acc = pre.dq_acc;
+    post.dq = static_cast<uint16_t*>(dq);
+    post.splits = D->splits;
+    post.part = p.part;
+    post.dk = p.dk;
+    post.dv = p.dv;
+    post.N = (int32_t)P->N;
+    post.hq = hq;
+    post.hkv = hkv;
+    post.d = d;
+    post.n_splits = (int32_t)(P->splits.size() / 4);
+    e = launch_bwd_post(post, s);
+    return e == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
+}
+
+int tree_attn_get_device_status(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return TREE_ATTN_ERR_CUDA;
+    int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess) return TREE_ATTN_ERR_CUDA;
+    if (v != 0 && cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) return TREE_ATTN_ERR_CUDA;
+    return v;
+}
+
+void tree_attn_plan_destroy(tree_attn_plan_t P) {
+    if (!P) return;
+    int cur = -1;
+    bool have = cudaGetDevice(&cur) == cudaSuccess;
+    for (int dev = 0; dev < kMaxDevices; ++dev) {
+        if (!P->dev[dev].ready) continue;
+        if (cudaSetDevice(dev) == cudaSuccess) cudaFree(P->dev[dev].base);
+    }
+    if (have) cudaSetDevice(cur);
+    cudaGetLastError();
+    delete P;
+}
+
+const char* tree_attn_strerror(int s) {
+    switch (s) {
+        case TREE_ATTN_OK: return "ok";
+        case TREE_ATTN_ERR_INVALID_ARG: return "invalid argument";
+        case TREE_ATTN_ERR_INVALID_TREE: return "invalid tree (parent out of range, self-parent, cycle or seg_len <= 0)";
+        case TREE_ATTN_ERR_TOO_LARGE: return "problem too large";
+        case TREE_ATTN_ERR_UNSUPPORTED: return "unsupported head configuration or block size";
+        case TREE_ATTN_ERR_ALIGNMENT: return "pointer not aligned (16 bytes; workspace 256 bytes)";
+        case TREE_ATTN_ERR_WORKSPACE: return "workspace missing or too small";
+        case TREE_ATTN_ERR_CUDA: return "CUDA runtime or driver error";
+        case TREE_ATTN_ERR_NO_DEVICE: return "no usable sm_103 device";
+        case TREE_ATTN_ERR_OUT_OF_MEMORY: return "out of memory";
+        default:
+            if (s <= TREE_ATTN_ERR_DEVICE_TIMEOUT) return "a bounded device wait ran out";
+            return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,354 @@
+// Backward kernel: dQ, dK, dV of tree attention on the sm_103a tensor cores.
+//
+// KV-major.  One CTA = one work item (kv-tile c, a chunk [t0, t1) of its
+// contiguous descendant q-range) x one kv-head.  The CTA keeps K_c and V_c in
+// shared memory and dV, dK in TMEM, and walks every step (q-tile t, q-head h
+// of the group) in a fixed order -- t ascending, then h ascending -- so dK and
+// dV are summed in the same order on every run.  Per step:
+//
+//   S^T  = K Q^T        (keys x queries, TMEM cols [0,128))
+//   dP^T = V dO^T       (TMEM cols [128,256))
+//   P^T  = exp2(S^T * scale*log2e - LSE*log2e)   masked: j <= i < subend[j]
+//   dS^T = P^T * (dP^T - Delta)                  (both written to smem, bf16)
+//   dV  += P^T dO       (TMEM cols [256, 256+D))
+//   dK  += dS^T Q       (TMEM cols [256+D, 256+2D))
+//   dQ   = dS K         (TMEM cols [0, D), reusing S^T), read out and added
+//                       to the fp32 dQ accumulator with vector reductions
+//
+// Warp roles (192 threads): warps 0-3 compute P^T / dS^T (one key row per
+// thread) and read dQ out (one query row per thread); warp 4 is the TMA
+// producer (K, V once; Q and dO per step through a ring; LSE and Delta rows by
+// bulk copy); warp 5 issues the MMAs and owns TMEM.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace treeattn {
+
+namespace {
+
+template <int D>
+struct BwdCfg {
+    static constexpr int TILE = 128 * D * 2;
+    static constexpr int PB = 128 * 128 * 2;
+    static constexpr int NSLOT = D == 128 ? 3 : 4;
+    static constexpr int SMALL = 3072;
+    static constexpr int OFF_K = SMALL;
+    static constexpr int OFF_V = OFF_K + TILE;
+    static constexpr int OFF_RING = OFF_V + TILE;
+    static constexpr int OFF_PT = OFF_RING + NSLOT * TILE;
+    static constexpr int OFF_DST = OFF_PT + PB;
+    static constexpr int BYTES = OFF_DST + PB;
+    static constexpr int NWARPS = 6;
+    static constexpr int PRODUCER = 4;
+    static constexpr int MMA = 5;
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D, T_DQ = 0;
+    // small region
+    static constexpr int B_KVFULL = 0;
+    static constexpr int B_FULL = 8;                     // [NSLOT]
+    static constexpr int B_EMPTY = B_FULL + 8 * NSLOT;   // [NSLOT]
+    static constexpr int B_LFULL = B_EMPTY + 8 * NSLOT;  // [2]
+    static constexpr int B_LEMPTY = B_LFULL + 16;        // [2]
+    static constexpr int B_SFULL = B_LEMPTY + 16;
+    static constexpr int B_PFULL = B_SFULL + 8;
+    static constexpr int B_DQFULL = B_PFULL + 8;
+    static constexpr int B_DQEMPTY = B_DQFULL + 8;
+    static constexpr int B_DKVFULL = B_DQEMPTY + 8;
+    static constexpr int B_DRAIN = B_DKVFULL + 8;
+    static constexpr int HOLDER = B_DRAIN + 8;
+    static constexpr int LSD = 1024;   // 2 stages x {lse2[128], delta[128]} fp32
+    static_assert(HOLDER + 4 <= LSD, "barriers");
+    static_assert(LSD + 2 * 1024 <= SMALL, "small region");
+    static_assert(BYTES <= 232448, "shared memory");
+};
+
+template <int D>
+__global__ void __launch_bounds__(BwdCfg<D>::NWARPS * 32, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+               const BwdParams p) {
+    using C = BwdCfg<D>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const uint32_t sb = smem_u32(smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (sb & 1023u) {
+        if (threadIdx.x == 0) report_status(p.status, -5);
+        return;
+    }
+    const int item = blockIdx.x / p.hkv;
+    const int hk = blockIdx.x % p.hkv;
+    const int4 it = reinterpret_cast<const int4*>(p.items)[item];
+    const int c = it.x, t0 = it.y, t1 = it.z, slot = it.w;
+    const int G = p.group;
+    const int nsteps = (t1 - t0) * G;
+
+    auto bar = [&](int off) { return sb + (uint32_t)off; };
+    if (threadIdx.x == 0) {
+        mbar_init(bar(C::B_KVFULL), 1);
+        for (int s = 0; s < C::NSLOT; ++s) {
+            mbar_init(bar(C::B_FULL + 8 * s), 1);
+            mbar_init(bar(C::B_EMPTY + 8 * s), 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(C::B_LFULL + 8 * s), 1);
+            mbar_init(bar(C::B_LEMPTY + 8 * s), 128);
+        }
+        mbar_init(bar(C::B_SFULL), 1);
+        mbar_init(bar(C::B_PFULL), 128);
+        mbar_init(bar(C::B_DQFULL), 1);
+        mbar_init(bar(C::B_DQEMPTY), 128);
+        mbar_init(bar(C::B_DKVFULL), 1);
+        mbar_init(bar(C::B_DRAIN), 1);
+        fence_mbar_init();
+    }
+    if (warp == C::MMA) tmem_alloc(sb + C::HOLDER, C::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::HOLDER);
+
+    if (warp == C::PRODUCER) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_do);
+            mbar_expect_tx(bar(C::B_KVFULL), 2 * C::TILE);
+            for (int blk = 0; blk < D / 64; ++blk) {
+                tma_load_3d(sb + C::OFF_K + blk * 16384, &tm_k, blk * 64, hk, c * 128, bar(C::B_KVFULL));
+                tma_load_3d(sb + C::OFF_V + blk * 16384, &tm_v, blk * 64, hk, c * 128, bar(C::B_KVFULL));
+            }
+            bool ok = true;
+            for (int n = 0; n < nsteps && ok; ++n) {
+                const int t = t0 + n / G, h = hk * G + n % G;
+                for (int w = 0; w < 2 && ok; ++w) {   // w = 0: Q, 1: dO
+                    const int pos = 2 * n + w, s = pos % C::NSLOT, use = pos / C::NSLOT;
+                    if (use > 0) ok = mbar_wait(bar(C::B_EMPTY + 8 * s), (use - 1) & 1, p.status, 21);
+                    if (!ok) break;
+                    mbar_expect_tx(bar(C::B_FULL + 8 * s), C::TILE);
+                    for (int blk = 0; blk < D / 64; ++blk)
+                        tma_load_3d(sb + C::OFF_RING + s * C::TILE + blk * 16384, w ? &tm_do : &tm_q, blk * 64, h,
+                                    t * 128, bar(C::B_FULL + 8 * s));
+                    if (w == 0) {
+                        const int ls = n & 1, luse = n >> 1;
+                        if (luse > 0) ok = mbar_wait(bar(C::B_LEMPTY + 8 * ls), (luse - 1) & 1, p.status, 22);
+                        if (!ok) break;
+                        mbar_expect_tx(bar(C::B_LFULL + 8 * ls), 1024);
+                        const size_t off = (size_t)h * p.Npad + (size_t)t * 128;
+                        bulk_load(sb + C::LSD + ls * 1024, p.lse2 + off, 512, bar(C::B_LFULL + 8 * ls));
+                        bulk_load(sb + C::LSD + ls * 1024 + 512, p.delta + off, 512, bar(C::B_LFULL + 8 * ls));
+                    }
+                }
+            }
+        }
+    } else if (warp == C::MMA) {
+        if (lane == 0) {
+            constexpr uint32_t ID_S = idesc_bf16(128, 128, false, false);   // K Q^T, V dO^T
+            constexpr uint32_t ID_KV = idesc_bf16(128, D, false, true);     // P^T dO, dS^T Q
+            constexpr uint32_t ID_Q = idesc_bf16(128, D, true, true);       // dS K
+            const uint32_t ka = sb + C::OFF_K, va = sb + C::OFF_V;
+            const uint32_t pta = sb + C::OFF_PT, dsa = sb + C::OFF_DST;
+            bool ok = mbar_wait(bar(C::B_KVFULL), 0, p.status, 23);
+            for (int n = 0; n < nsteps && ok; ++n) {
+                const int qpos = 2 * n, qs = qpos % C::NSLOT;
+                const int dpos = 2 * n + 1, ds = dpos % C::NSLOT;
+                ok = mbar_wait(bar(C::B_FULL + 8 * qs), (qpos / C::NSLOT) & 1, p.status, 24);
+                if (ok) ok = mbar_wait(bar(C::B_FULL + 8 * ds), (dpos / C::NSLOT) & 1, p.status, 25);
+                if (ok && n > 0) ok = mbar_wait(bar(C::B_DQEMPTY), (n - 1) & 1, p.status, 26);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t qa = sb + C::OFF_RING + qs * C::TILE, doa = sb + C::OFF_RING + ds * C::TILE;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+                    mma_bf16_ss(tmem + C::T_S, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024), ID_S,
+                                k > 0);
+                }
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+                    mma_bf16_ss(tmem + C::T_DP, sdesc_sw128(va + off, 16, 1024), sdesc_sw128(doa + off, 16, 1024),
+                                ID_S, k > 0);
+                }
+                mma_commit(bar(C::B_SFULL));
+                ok = mbar_wait(bar(C::B_PFULL), n & 1, p.status, 27);
+                if (!ok) break;
+                tc_fence_after();
+                // dV += P^T dO ; dK += dS^T Q   (K dimension = 128 queries)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t aoff = (k >> 2) * 16384 + (k & 3) * 32;
+                    mma_bf16_ss(tmem + C::T_DV, sdesc_sw128(pta + aoff, 16, 1024),
+                                sdesc_sw128(doa + k * 2048, 16384, 1024), ID_KV, (n > 0 || k > 0) ? 1u : 0u);
+                }
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t aoff = (k >> 2) * 16384 + (k & 3) * 32;
+                    mma_bf16_ss(tmem + C::T_DK, sdesc_sw128(dsa + aoff, 16, 1024),
+                                sdesc_sw128(qa + k * 2048, 16384, 1024), ID_KV, (n > 0 || k > 0) ? 1u : 0u);
+                }
+                // dQ = dS K   (M = queries, K dimension = 128 keys; both operands MN-major)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    mma_bf16_ss(tmem + C::T_DQ, sdesc_sw128(dsa + k * 2048, 16384, 1024),
+                                sdesc_sw128(ka + k * 2048, 16384, 1024), ID_Q, k > 0);
+                }
+                mma_commit(bar(C::B_DQFULL));
+                mma_commit(bar(C::B_EMPTY + 8 * qs));
+                mma_commit(bar(C::B_EMPTY + 8 * ds));
+            }
+            if (ok) mma_commit(bar(C::B_DKVFULL));
+            mma_commit(bar(C::B_DRAIN));
+            mbar_wait(bar(C::B_DRAIN), 0, p.status, 28);
+        }
+        __syncwarp();
+    } else {
+        // --------------------- P^T / dS^T, then dQ readout ---------------------
+        const int r = (warp << 5) + lane;            // TMEM lane
+        const uint32_t lane_base = tmem + ((uint32_t)(warp << 5) << 16);
+        const int j = c * 128 + r;                   // this thread's key
+        const int sub_j = p.subend[j];               // 0 past N
+        const float sl2 = p.scale_log2;
+        const uint32_t pta = sb + C::OFF_PT, dsa = sb + C::OFF_DST;
+        bool ok = true;
+        for (int n = 0; n < nsteps && ok; ++n) {
+            const int t = t0 + n / G, h = hk * G + n % G;
+            const int q0 = t * 128;
+            const int lo = max(j - q0, 0), hi = min(sub_j - q0, 128);
+            const int ls = n & 1;
+            ok = mbar_wait(bar(C::B_LFULL + 8 * ls), (n >> 1) & 1, p.status, 29);
+            if (ok) ok = mbar_wait(bar(C::B_SFULL), n & 1, p.status, 30);
+            if (!ok) break;
+            tc_fence_after();
+            const float4* lse4 = reinterpret_cast<const float4*>(smem + C::LSD + ls * 1024);
+            const float4* del4 = reinterpret_cast<const float4*>(smem + C::LSD + ls * 1024 + 512);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                float sv[32], dp[32];
+                tmem_ld32(lane_base + C::T_S + cc * 32, sv);
+                tmem_ld32(lane_base + C::T_DP + cc * 32, dp);
+                tmem_wait_ld();
+                uint32_t pw[16], dw[16];
+#pragma unroll
+                for (int u4 = 0; u4 < 8; ++u4) {
+                    const float4 l4 = lse4[cc * 8 + u4];
+                    const float4 d4 = del4[cc * 8 + u4];
+                    const float la[4] = {l4.x, l4.y, l4.z, l4.w};
+                    const float da[4] = {d4.x, d4.y, d4.z, d4.w};
+                    float pv[4], dv[4];
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const int u = u4 * 4 + w;
+                        const int col = cc * 32 + u;
+                        float pe = fast_exp2(fmaf(sv[u], sl2, -la[w]));
+                        pe = (col >= lo && col < hi) ? pe : 0.f;
+                        pv[w] = pe;
+                        dv[w] = pe * (dp[u] - da[w]);
+                    }
+                    pw[u4 * 2] = pack_bf16x2(pv[0], pv[1]);
+                    pw[u4 * 2 + 1] = pack_bf16x2(pv[2], pv[3]);
+                    dw[u4 * 2] = pack_bf16x2(dv[0], dv[1]);
+                    dw[u4 * 2 + 1] = pack_bf16x2(dv[2], dv[3]);
+                }
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    const int col = cc * 32 + g * 8;
+                    const uint32_t off = (col >> 6) * 16384 + sw128_offset(r, (col & 63) >> 3);
+                    st_shared_v4(pta + off, pw[4 * g], pw[4 * g + 1], pw[4 * g + 2], pw[4 * g + 3]);
+                    st_shared_v4(dsa + off, dw[4 * g], dw[4 * g + 1], dw[4 * g + 2], dw[4 * g + 3]);
+                }
+            }
+            mbar_arrive(bar(C::B_LEMPTY + 8 * ls));
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(C::B_PFULL));
+            // dQ rows: this thread's TMEM lane is now query q0 + r
+            ok = mbar_wait(bar(C::B_DQFULL), n & 1, p.status, 31);
+            if (!ok) break;
+            tc_fence_after();
+            const int i = q0 + r;
+            float* dst = p.dq_acc + ((size_t)i * p.hq + h) * D;
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+                float v[32];
+                tmem_ld32(lane_base + C::T_DQ + cc * 32, v);
+                tmem_wait_ld();
+                if (i < p.N) {
+#pragma unroll
+                    for (int u = 0; u < 32; u += 4)
+                        red_add_v4(dst + cc * 32 + u, v[u] * p.scale, v[u + 1] * p.scale, v[u + 2] * p.scale,
+                                   v[u + 3] * p.scale);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar(C::B_DQEMPTY));
+        }
+        // ------------------------------ dK, dV ---------------------------------
+        if (ok) ok = mbar_wait(bar(C::B_DKVFULL), 0, p.status, 32);
+        if (ok) {
+            tc_fence_after();
+            for (int which = 0; which < 2; ++which) {   // 0: dK, 1: dV
+                const uint32_t tcol = which == 0 ? C::T_DK : C::T_DV;
+                const float mul = which == 0 ? p.scale : 1.f;
+                if (slot < 0) {
+                    uint16_t* out = (which == 0 ? p.dk : p.dv) + ((size_t)j * p.hkv + hk) * D;
+#pragma unroll
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        float v[32];
+                        tmem_ld32(lane_base + tcol + cc * 32, v);
+                        tmem_wait_ld();
+                        if (j < p.N) {
+#pragma unroll
+                            for (int u = 0; u < 32; u += 8) {
+                                uint4 w;
+                                w.x = pack_bf16x2(v[u] * mul, v[u + 1] * mul);
+                                w.y = pack_bf16x2(v[u + 2] * mul, v[u + 3] * mul);
+                                w.z = pack_bf16x2(v[u + 4] * mul, v[u + 5] * mul);
+                                w.w = pack_bf16x2(v[u + 6] * mul, v[u + 7] * mul);
+                                *reinterpret_cast<uint4*>(out + cc * 32 + u) = w;
+                            }
+                        }
+                    }
+                } else {
+                    float* out = p.part + ((((size_t)slot * p.hkv + hk) * 2 + which) * 128 + r) * D;
+#pragma unroll
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        float v[32];
+                        tmem_ld32(lane_base + tcol + cc * 32, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int u = 0; u < 32; u += 4)
+                            *reinterpret_cast<float4*>(out + cc * 32 + u) =
+                                make_float4(v[u] * mul, v[u + 1] * mul, v[u + 2] * mul, v[u + 3] * mul);
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == C::MMA) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+template <int D>
+cudaError_t launch_cfg(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv, const CUtensorMap* tdo,
+                       const BwdParams& p, int grid, cudaStream_t stream) {
+    using C = BwdCfg<D>;
+    auto kern = bwd_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, C::NWARPS * 32, C::BYTES, stream>>>(*tq, *tk, *tv, *tdo, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(int d, const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
+                       const CUtensorMap* tdo, const BwdParams& p, int grid, cudaStream_t stream) {
+    if (grid <= 0) return cudaSuccess;
+    return d == 128 ? launch_cfg<128>(tq, tk, tv, tdo, p, grid, stream)
+                    : launch_cfg<64>(tq, tk, tv, tdo, p, grid, stream);
+}
+
+}  // namespace treeattn

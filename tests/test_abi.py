@@ -1,0 +1,99 @@
+"""The C-ABI library loads, exports every symbol include/tree_attn.h declares,
+and rejects bad arguments on the host (CPU only; no compute call is made)."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+from prefix_tree_attention_attn_gb300 import _binding as B
+from prefix_tree_attention_attn_gb300 import TreePlan
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "tree_attn.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tree_attn_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in B.SIGNATURES, n
+
+
+def test_status_codes_named(lib):
+    text = open(HEADER).read()
+    codes = {int(v) for v in re.findall(r"#define TREE_ATTN_(?:OK|ERR_[A-Z_]+)\s+(-?\d+)", text)}
+    assert codes == set(range(-10, 1))
+    for code in codes:
+        s = lib.tree_attn_strerror(code).decode()
+        assert s and s != "unknown status"
+    assert lib.tree_attn_strerror(-10 - 1000 * 5).decode().startswith("a bounded device wait")
+
+
+def plan_status(lib, parent, seg_len, block=0, chunk=0):
+    par = np.asarray(parent, dtype=np.int32)
+    sl = np.asarray(seg_len, dtype=np.int32)
+    h = C.c_void_p()
+    opts = B.PlanOpts(block, chunk)
+    st = lib.tree_attn_plan(par.ctypes.data_as(B.c_int32_p), sl.ctypes.data_as(B.c_int32_p), len(par),
+                            C.byref(opts), C.byref(h))
+    if st == 0:
+        lib.tree_attn_plan_destroy(h)
+    return st
+
+
+@pytest.mark.parametrize("parent,seg_len,code", [
+    ([-1, 0], [3, 0], -2),            # empty segment
+    ([-1, 0], [3, -1], -2),
+    ([0], [3], -2),                   # self parent
+    ([-1, 5], [3, 3], -2),            # parent out of range
+    ([-1, -2], [3, 3], -2),
+    ([1, 0], [2, 2], -2),             # cycle, no root
+    ([-1, 2, 1], [1, 2, 2], -2),      # cycle beside a root
+    ([], [], -1),
+])
+def test_invalid_trees_rejected(lib, parent, seg_len, code):
+    assert plan_status(lib, parent, seg_len) == code
+
+
+def test_invalid_options_and_sizes(lib):
+    assert plan_status(lib, [-1], [4], block=-3) == -1
+    assert plan_status(lib, [-1], [4], block=2048) == -1
+    assert plan_status(lib, [-1], [4], chunk=-1) == -1
+    assert plan_status(lib, [-1, 0], [2**30, 2**30]) == -3      # token count overflows int32
+    h = C.c_void_p()
+    assert lib.tree_attn_plan(None, None, 1, None, C.byref(h)) == -1
+    assert lib.tree_attn_plan_info(None, None) == -1
+    assert lib.tree_attn_plan_export(None, None) == -1
+
+
+def test_compute_calls_validate_before_touching_the_device(lib):
+    p = TreePlan([-1, 0], [100, 60])
+    # null tensors -> invalid argument, checked on the host first
+    assert lib.tree_attn_fwd(p.handle, None, None, None, None, None, 2, 2, 64, 1.0, None, 0, None) == -1
+    assert lib.tree_attn_bwd(p.handle, None, None, None, None, None, None, None, None, None,
+                             2, 2, 64, 1.0, None, 0, None) == -1
+    # unsupported head configurations
+    f, b = C.c_size_t(), C.c_size_t()
+    assert lib.tree_attn_workspace_size(p.handle, 3, 2, 64, C.byref(f), C.byref(b)) == -4
+    assert lib.tree_attn_workspace_size(p.handle, 4, 2, 96, C.byref(f), C.byref(b)) == -4
+    assert lib.tree_attn_workspace_size(p.handle, 4, 2, 128, C.byref(f), C.byref(b)) == 0
+    assert f.value == 0 and b.value > 0
+    p64 = TreePlan([-1, 0], [100, 60], block=64)
+    assert lib.tree_attn_workspace_size(p64.handle, 4, 2, 128, C.byref(f), C.byref(b)) == -4
+    # misaligned device pointers are refused before any launch
+    fake = C.c_void_p(0x1000)
+    odd = C.c_void_p(0x1008)
+    assert lib.tree_attn_fwd(p.handle, odd, fake, fake, fake, fake, 2, 2, 64, 1.0, None, 0, None) == -5
+    assert lib.tree_attn_fwd(p.handle, fake, fake, fake, fake, fake, 2, 2, 64, float("nan"),
+                             None, 0, None) == -1
+    # workspace too small
+    assert lib.tree_attn_bwd(p.handle, fake, fake, fake, fake, fake, fake, fake, fake, fake,
+                             2, 2, 64, 1.0, fake, 16, None) == -6

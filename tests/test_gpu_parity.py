@@ -1,0 +1,100 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle, on
+seeded inputs, element by element (forward: max / mean abs error; backward:
+relative Frobenius error per tensor)."""
+import numpy as np
+import pytest
+import torch
+
+from prefix_tree_attention_attn_gb300 import TreePlan, device_status, tree_attn_bwd, tree_attn_fwd
+from workloads import tensors as WX
+from workloads import trees as WT
+
+from .gpu_util import assert_bwd, assert_fwd, full_parity, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def draw(N, hq, hkv, d, seed, qk_std=1.0, do_std=1.0):
+    rec = WX.ValueRecipe(qk_std, qk_std, 1.0, do_std, 1.0)
+    x = WX.draw_inputs(N, WX.HeadConfig(hq, hkv, d), rec, seed)
+    return x["q"], x["k"], x["v"], x["do"]
+
+
+@pytest.fixture(autouse=True)
+def _lib(lib, cuda_device):
+    yield
+    assert device_status() == 0
+
+
+# --------------------------------------------------------------------------
+# small cases: several tiles, ragged tails, every head layout
+# --------------------------------------------------------------------------
+
+SMALL = [
+    # (parent, seg_len, hq, hkv, d)
+    ([-1], [1], 2, 2, 64),                                   # one token
+    ([-1], [200], 2, 1, 128),                                # single chain, ragged tail
+    ([-1, 0, 0], [127, 129, 1], 4, 2, 128),                  # adversarial lengths
+    ([-1, 0, 0, 1, 1], [128, 128, 255, 1, 129], 8, 2, 128),  # group 4
+    ([-1, 0, 1, -1, 3], [70, 60, 5, 300, 2], 3, 3, 64),      # forest, group 1 (odd)
+    ([-1, 0, 0, 0, 0, 0], [256, 40, 1, 129, 300, 7], 6, 2, 64),  # group 3 (odd)
+]
+
+
+@pytest.mark.parametrize("case", range(len(SMALL)))
+def test_small_trees(case):
+    parent, seg_len, hq, hkv, d = SMALL[case]
+    t = WT.Tree("small", parent, seg_len)
+    q, k, v, do = draw(t.n_tokens, hq, hkv, d, seed=case)
+    full_parity(t, q, k, v, do, 1 / np.sqrt(d), tag=f"case{case}")
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_random_trees(seed):
+    rng = np.random.default_rng(77 + seed)
+    t = WT.random_tree(rng, int(rng.integers(3, 14)), [1, 17, 64, 127, 128, 129, 255, 300],
+                       n_roots=1 + seed % 2)
+    hq, hkv, d = [(4, 4, 128), (8, 2, 128), (4, 2, 64), (2, 1, 128)][seed]
+    q, k, v, do = draw(t.n_tokens, hq, hkv, d, seed=100 + seed)
+    full_parity(t, q, k, v, do, 1 / np.sqrt(d), tag=f"seed{seed}")
+
+
+def test_sharp_logits():
+    """Unscaled N(0,1) q/k with a large softmax scale: peaked rows, which
+    exercise the O rescaling when the running maximum jumps."""
+    t = WT.Tree("sharp", [-1, 0, 0], [300, 200, 260])
+    q, k, v, do = draw(t.n_tokens, 4, 2, 128, seed=9)
+    full_parity(t, q, k, v, do, 0.35, tag="sharp")
+
+
+# --------------------------------------------------------------------------
+# the workload trees
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["tiny_binary", "tiny_binary_sharp"])
+def test_tiny_binary_tree(name):
+    t = WT.load_tree("tiny_binary")
+    heads, rec, x = WX.workload_inputs(name, t.n_tokens)
+    full_parity(t, x["q"], x["k"], x["v"], x["do"], rec.scale, tag=name)
+
+
+@pytest.mark.parametrize("name", ["grpo_star", "segment_tree"])
+def test_medium_workloads_full(name):
+    t = WT.load_tree(name)
+    heads, rec, x = WX.workload_inputs(name, t.n_tokens)
+    full_parity(t, x["q"], x["k"], x["v"], x["do"], rec.scale, tag=name)
+
+
+def test_backward_dk_dv_bitwise_reproducible():
+    t = WT.load_tree("segment_tree")
+    heads, rec, x = WX.workload_inputs("segment_tree", t.n_tokens)
+    plan = TreePlan(t.parent, t.seg_len)
+    dev = torch.device("cuda:0")
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    o, lse = tree_attn_fwd(plan, q, k, v, rec.scale)
+    o2, lse2 = tree_attn_fwd(plan, q, k, v, rec.scale)
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    _, dk1, dv1 = tree_attn_bwd(plan, q, k, v, o, lse, do, rec.scale)
+    _, dk2, dv2 = tree_attn_bwd(plan, q, k, v, o, lse, do, rec.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)

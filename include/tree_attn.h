@@ -151,6 +151,22 @@ int tree_attn_bwd(tree_attn_plan_t plan, const void* q, const void* k, const voi
                   void* dq, void* dk, void* dv, int32_t hq, int32_t hkv, int32_t d,
                   float softmax_scale, void* workspace, size_t ws_bytes, void* stream);
 
+/* The backward in stages (the same arguments as tree_attn_bwd, plus a mask):
+ *   TREE_ATTN_BWD_PRE  -- Delta = rowsum(dO * O), LSE in log2 units, zero the
+ *                         fp32 dQ accumulator (memory-bound)
+ *   TREE_ATTN_BWD_MAIN -- the tensor-core pass over (kv-tile, q-tile) blocks
+ *   TREE_ATTN_BWD_POST -- dQ to bf16; fixed-order sum of split dK/dV partials
+ * Stages must run in this order, on one stream, with one workspace;
+ * tree_attn_bwd is all three.  Lets a caller time or overlap each stage. */
+#define TREE_ATTN_BWD_PRE  1
+#define TREE_ATTN_BWD_MAIN 2
+#define TREE_ATTN_BWD_POST 4
+int tree_attn_bwd_stages(tree_attn_plan_t plan, const void* q, const void* k, const void* v,
+                         const void* o, const float* lse, const void* dout,
+                         void* dq, void* dk, void* dv, int32_t hq, int32_t hkv, int32_t d,
+                         float softmax_scale, void* workspace, size_t ws_bytes, void* stream,
+                         int32_t stages);
+
 /* Synchronise `stream`, then read and clear the device status word of the
  * current device: 0 when every kernel's bounded waits finished in time,
  * otherwise TREE_ATTN_ERR_DEVICE_TIMEOUT - 1000 * (site of the wait) or

@@ -138,9 +138,15 @@ def tree_attn_fwd(plan: TreePlan, q, k, v, softmax_scale: float, o=None, lse=Non
     return o, lse
 
 
+BWD_PRE, BWD_MAIN, BWD_POST = 1, 2, 4
+
+
 def tree_attn_bwd(plan: TreePlan, q, k, v, o, lse, dout, softmax_scale: float, dq=None, dk=None, dv=None,
-                  workspace=None, stream=None):
-    """dQ, dK, dV (bf16) from the forward's O and LSE and the output gradient."""
+                  workspace=None, stream=None, stages: int = 7):
+    """dQ, dK, dV (bf16) from the forward's O and LSE and the output gradient.
+    ``stages`` (bit mask of BWD_PRE / BWD_MAIN / BWD_POST) runs part of the
+    backward (``tree_attn_bwd_stages``); stages must run in order with one
+    workspace."""
     import torch
     N, hq, d = q.shape
     hkv = k.shape[1]
@@ -154,9 +160,10 @@ def tree_attn_bwd(plan: TreePlan, q, k, v, o, lse, dout, softmax_scale: float, d
     _, need = plan.workspace_size(hq, hkv, d)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
-    B.check(B.load().tree_attn_bwd(plan.handle, _dptr(q), _dptr(k), _dptr(v), _dptr(o), _dptr(lse), _dptr(dout),
-                                   _dptr(dq), _dptr(dk), _dptr(dv), hq, hkv, d, float(softmax_scale),
-                                   _dptr(workspace), workspace.numel(), _stream_ptr(stream)), "tree_attn_bwd")
+    B.check(B.load().tree_attn_bwd_stages(plan.handle, _dptr(q), _dptr(k), _dptr(v), _dptr(o), _dptr(lse),
+                                          _dptr(dout), _dptr(dq), _dptr(dk), _dptr(dv), hq, hkv, d,
+                                          float(softmax_scale), _dptr(workspace), workspace.numel(),
+                                          _stream_ptr(stream), int(stages)), "tree_attn_bwd_stages")
     return dq, dk, dv
 
 

@@ -276,6 +276,15 @@ int tree_attn_fwd(tree_attn_plan_t P, const void* q, const void* k, const void* 
 int tree_attn_bwd(tree_attn_plan_t P, const void* q, const void* k, const void* v, const void* o, const float* lse,
                   const void* dout, void* dq, void* dk, void* dv, int32_t hq, int32_t hkv, int32_t d,
                   float softmax_scale, void* workspace, size_t ws_bytes, void* stream) {
+    return tree_attn_bwd_stages(P, q, k, v, o, lse, dout, dq, dk, dv, hq, hkv, d, softmax_scale, workspace, ws_bytes,
+                                stream, TREE_ATTN_BWD_PRE | TREE_ATTN_BWD_MAIN | TREE_ATTN_BWD_POST);
+}
+
+int tree_attn_bwd_stages(tree_attn_plan_t P, const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dout, void* dq, void* dk, void* dv, int32_t hq, int32_t hkv,
+                         int32_t d, float softmax_scale, void* workspace, size_t ws_bytes, void* stream,
+                         int32_t stages) {
+    if (stages <= 0 || stages > 7) return TREE_ATTN_ERR_INVALID_ARG;
     if (!P || !q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return TREE_ATTN_ERR_INVALID_ARG;
     if (!std::isfinite(softmax_scale)) return TREE_ATTN_ERR_INVALID_ARG;
     int st = check_heads(P, hq, hkv, d);
@@ -307,8 +316,11 @@ int tree_attn_bwd(tree_attn_plan_t P, const void* q, const void* k, const void* 
     pre.Npad = Npad;
     pre.hq = hq;
     pre.d = d;
-    cudaError_t e = launch_bwd_pre(pre, s);
-    if (e != cudaSuccess) return TREE_ATTN_ERR_CUDA;
+    cudaError_t e = cudaSuccess;
+    if (stages & TREE_ATTN_BWD_PRE) {
+        e = launch_bwd_pre(pre, s);
+        if (e != cudaSuccess) return TREE_ATTN_ERR_CUDA;
+    }
 
     BwdParams p;
     p.items = D->bwd_items;
@@ -332,8 +344,10 @@ int tree_attn_bwd(tree_attn_plan_t P, const void* q, const void* k, const void* 
     if ((st = status_ptr(dev, &p.status))) return st;
     const int64_t n_items = (int64_t)P->bwd_items.size() / 4;
     if (n_items * hkv > INT32_MAX) return TREE_ATTN_ERR_TOO_LARGE;
-    e = launch_bwd(d, &tq, &tk, &tv, &tdo, p, (int)(n_items * hkv), s);
-    if (e != cudaSuccess) return TREE_ATTN_ERR_CUDA;
+    if (stages & TREE_ATTN_BWD_MAIN) {
+        e = launch_bwd(d, &tq, &tk, &tv, &tdo, p, (int)(n_items * hkv), s);
+        if (e != cudaSuccess) return TREE_ATTN_ERR_CUDA;
+    }
 
     BwdPostParams post;
     post.dq_acc = pre.dq_acc;
@@ -347,7 +361,7 @@ int tree_attn_bwd(tree_attn_plan_t P, const void* q, const void* k, const void* 
     post.hkv = hkv;
     post.d = d;
     post.n_splits = (int32_t)(P->splits.size() / 4);
-    e = launch_bwd_post(post, s);
+    if (stages & TREE_ATTN_BWD_POST) e = launch_bwd_post(post, s);
     return e == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
 }
 

@@ -1,0 +1,429 @@
+#!/usr/bin/env python
+"""Benchmark: prefix-tree attention forward + backward on GB300.
+
+One step = one pass of the whole hot path over the synthetic GRPO-style star
+tree (a 1024-token prompt shared by 16 responses of U[256, 1024] tokens;
+32 query heads, 8 kv heads, head_dim 128, bf16): the forward kernel, then the
+backward's three stages.  The metric is useful TFLOP/s, counting only
+attended (ancestor) pairs: 4*d per pair and q-head forward, 10*d backward.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
+oracle instead, on a bounded sample of the same workload.
+
+    python bench.py [--gpus N --steps K --warmup W] [--workload NAME] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "tree-attn fwd+bwd useful TFLOP/s (ancestor pairs) and % of bf16 TC peak, 1 GB300"
+UNIT = "TFLOP/s"
+L2_FLUSH_BYTES = 512 << 20          # larger than the 129 MB L2
+FALLBACK_BF16_TFLOPS = 1900.0
+
+DESCRIPTIONS = {
+    "grpo_star": "GRPO-style star tree: 1024-token prompt + 16 responses U[256,1024]; 32q/8kv heads, d=128",
+    "segment_tree": "segment tree: 512-token prompt, 256-token segments, binary x4, early stop + fallback "
+                    "to 16 leaves; 32q/8kv heads, d=128",
+    "agentic_tree": "irregular agentic tree ~64k compact tokens, 4-6x expansion; 32q/8kv heads, d=128",
+    "tiny_binary": "tiny binary tree 64 + 2x32 + 4x32 tokens; 2 heads, d=64",
+    "long_context": "long shared context: 32768-token prefix + 64 chains of 1-3 log-U[1k,8k] segments; "
+                    "64q/8kv heads, d=128",
+}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="grpo_star")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-expanded", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the CPU sample")
+    return ap.parse_args()
+
+
+def useful_flops(pairs: int, hq: int, d: int):
+    return 4.0 * d * pairs * hq, 10.0 * d * pairs * hq
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["bf16_tflops"]), float(j.get("bf16_tflops_sustained", j["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "prefix_tree_attention_attn_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str, src_hash: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (same hash); else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 4 and parts[0] == kernel and parts[1] == workload and parts[2] == src_hash:
+            return float(parts[3])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.index), "-lms", "100"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the oracle on a bounded sample (CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample_step(tree, x, heads, scale, groups):
+    """fp64 oracle forward + backward on kv-groups ``groups`` (their q-heads
+    and kv-head) of the workload; returns the useful FLOPs it covers."""
+    from oracle import attention as OA
+    G = heads.group
+    pairs = None
+    flops = 0.0
+    for g in groups:
+        qs = slice(g * G, (g + 1) * G)
+        q, k, v, do = x["q"][:, qs], x["k"][:, g:g + 1], x["v"][:, g:g + 1], x["do"][:, qs]
+        OA.forward(tree.parent, tree.seg_len, q, k, v, scale, check_copies=False)
+        OA.backward(tree.parent, tree.seg_len, q, k, v, do, scale)
+        if pairs is None:
+            from oracle import plan as OP
+            pairs = OP.pair_count(tree.parent, tree.seg_len)
+        flops += 14.0 * heads.d * pairs * G
+    return flops
+
+
+def cpu_baseline(tree, x, heads, scale, target_s):
+    """Time the oracle as it stands on one kv-group at a time until about
+    ``target_s`` seconds have been spent."""
+    t0 = time.perf_counter()
+    flops, groups = 0.0, 0
+    while groups < heads.hkv:
+        flops += oracle_sample_step(tree, x, heads, scale, [groups])
+        groups += 1
+        if time.perf_counter() - t0 >= target_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"fp64 numpy oracle, fwd+bwd of {groups} of {heads.hkv} kv-head groups "
+                      f"({groups * heads.group} q-heads) of the full tree, {dt:.1f} s; numpy BLAS default threads"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from workloads import tensors as WX
+    from workloads import trees as WT
+    tree = WT.load_tree(args.workload)
+    heads, rec, x = WX.workload_inputs(args.workload, tree.n_tokens)
+    for _ in range(args.warmup):
+        oracle_sample_step(tree, x, heads, rec.scale, [0])
+    times, flops = [], 0.0
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        flops = oracle_sample_step(tree, x, heads, rec.scale, [0])
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = flops * args.steps / total / 1e12
+    sample = (f"fp64 numpy oracle fwd+bwd on kv-head group 0 ({heads.group} q-heads, 1 kv-head) of "
+              f"the full tree per step")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": DESCRIPTIONS.get(args.workload, args.workload),
+                                        "name": args.workload, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }))
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import prefix_tree_attention_attn_gb300 as TA
+    from workloads import tensors as WX
+    from workloads import trees as WT
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    tree = WT.load_tree(args.workload)
+    heads, rec, x = WX.workload_inputs(args.workload, tree.n_tokens)
+    hq, hkv, d, scale = heads.hq, heads.hkv, heads.d, rec.scale
+    plan = TA.TreePlan(tree.parent, tree.seg_len)
+    N = plan.n_tokens
+    f_fwd, f_bwd = useful_flops(plan.n_pairs, hq, d)
+    flops_step = f_fwd + f_bwd
+
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty((hq, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(max(plan.workspace_size(hq, hkv, d)[1], 1), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    n_splits = plan.info["n_split_kv_tiles"]
+    launches_per_step = 1 + 1 + 1 + 1 + (1 if n_splits > 0 else 0)
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        TA.tree_attn_fwd(plan, q, k, v, scale, o=o, lse=lse)
+        if evs:
+            evs[1].record(stream)
+        TA.tree_attn_bwd(plan, q, k, v, o, lse, do, scale, dq=dq, dk=dk, dv=dv, workspace=ws,
+                         stages=TA.BWD_PRE)
+        if evs:
+            evs[2].record(stream)
+        TA.tree_attn_bwd(plan, q, k, v, o, lse, do, scale, dq=dq, dk=dk, dv=dv, workspace=ws,
+                         stages=TA.BWD_MAIN)
+        if evs:
+            evs[3].record(stream)
+        TA.tree_attn_bwd(plan, q, k, v, o, lse, do, scale, dq=dq, dk=dk, dv=dv, workspace=ws,
+                         stages=TA.BWD_POST)
+        if evs:
+            evs[4].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    if TA.device_status() != 0:
+        raise RuntimeError("device status non-zero after warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)                        # let the sampler start
+    barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for kk in range(args.steps):
+        flush.fill_(kk & 0xff)             # evict L2 between timed steps (not timed)
+        step(evs[kk])
+    torch.cuda.synchronize()
+    barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    status = TA.device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status}")
+
+    per = [[e[i].elapsed_time(e[i + 1]) for i in range(4)] for e in evs]   # fwd, pre, main, post (ms)
+    step_ms = [sum(p) for p in per]
+    total_ms = sum(step_ms)
+    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_max_ms = float(t.item())
+    value = flops_step * args.steps * world / (total_max_ms / 1e3) / 1e12
+    fwd_ms = statistics.mean(p[0] for p in per)
+    main_ms = statistics.mean(p[2] for p in per)
+    pre_ms = statistics.mean(p[1] for p in per)
+    post_ms = statistics.mean(p[3] for p in per)
+
+    peak_burst, peak_sus, peak_src = measured_peaks()
+    dominant = ("bwd_kernel", main_ms, f_bwd) if main_ms >= fwd_ms else ("fwd_kernel", fwd_ms, f_fwd)
+    achieved = dominant[2] / (dominant[1] / 1e3) / 1e12
+    src_hash = kernel_source_hash(["bwd.cu" if dominant[0] == "bwd_kernel" else "fwd.cu", "ptx.cuh"])
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_burst, "unit": "TFLOP/s",
+                "frac": achieved / peak_burst, "traffic": recorded_traffic(dominant[0], args.workload, src_hash),
+                "kernel": dominant[0], "peak_source": f"{peak_src} bf16 burst",
+                "kernel_src_hash": src_hash}
+
+    # ---- end to end through the public API, host buffers ------------------
+    e2e = None
+    if rank == 0 or world > 1:
+        pin = {n: x[n].pin_memory() for n in ("q", "k", "v", "do")}
+        outs = {"o": torch.empty(o.shape, dtype=o.dtype, pin_memory=True),
+                "lse": torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True),
+                "dq": torch.empty(dq.shape, dtype=dq.dtype, pin_memory=True),
+                "dk": torch.empty(dk.shape, dtype=dk.dtype, pin_memory=True),
+                "dv": torch.empty(dv.shape, dtype=dv.dtype, pin_memory=True)}
+        h2d = sum(t_.numel() * t_.element_size() for t_ in pin.values())
+        d2h = sum(t_.numel() * t_.element_size() for t_ in outs.values())
+        e2e_steps = max(3, min(args.steps, 20))
+
+        def e2e_step():
+            p2 = TA.TreePlan(tree.parent, tree.seg_len)        # a new tree each step: plan on the host
+            qd, kd, vd, dod = (pin[n].to(dev, non_blocking=True) for n in ("q", "k", "v", "do"))
+            oo, ll = TA.tree_attn_fwd(p2, qd, kd, vd, scale)
+            a, b, c = TA.tree_attn_bwd(p2, qd, kd, vd, oo, ll, dod, scale)
+            for name, src in (("o", oo), ("lse", ll), ("dq", a), ("dk", b), ("dv", c)):
+                outs[name].copy_(src, non_blocking=True)
+            torch.cuda.synchronize()
+            p2.close()
+
+        e2e_step()
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            e2e_step()
+        e2e_s = (time.perf_counter() - t0) / e2e_steps
+        e2e = {"value": flops_step * world / e2e_s / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3,
+               "includes": "host plan build + device upload, H2D of q/k/v/dO from pinned memory, fwd+bwd, "
+                           "D2H of o/lse/dq/dk/dv"}
+
+    # ---- same kernels on the expanded trajectories ---------------------------
+    expanded = None
+    if not args.no_expanded and rank == 0:
+        ft = WT.expanded_forest(tree)
+        fp = TA.TreePlan(ft.parent, ft.seg_len)
+        Ne = fp.n_tokens
+        g = torch.Generator(device=dev)
+        g.manual_seed(7)
+        xe = {n: (torch.randn((Ne, h, d), generator=g, device=dev, dtype=torch.float32)).to(torch.bfloat16)
+              for n, h in (("q", hq), ("k", hkv), ("v", hkv), ("do", hq))}
+        wse = torch.empty(max(fp.workspace_size(hq, hkv, d)[1], 1), dtype=torch.uint8, device=dev)
+
+        def estep():
+            oo, ll = TA.tree_attn_fwd(fp, xe["q"], xe["k"], xe["v"], scale)
+            TA.tree_attn_bwd(fp, xe["q"], xe["k"], xe["v"], oo, ll, xe["do"], scale, workspace=wse)
+
+        for _ in range(3):
+            estep()
+        torch.cuda.synchronize()
+        ee = []
+        for _ in range(min(args.steps, 20)):
+            flush.fill_(3)
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_.record()
+            estep()
+            b_.record()
+            ee.append((a_, b_))
+        torch.cuda.synchronize()
+        ems = statistics.mean(a_.elapsed_time(b_) for a_, b_ in ee)
+        expanded = {"ms_per_step": ems, "speedup": ems / (total_ms / args.steps), "n_tokens": Ne,
+                    "pairs": fp.n_pairs}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(tree, x, heads, scale, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": total_max_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": DESCRIPTIONS.get(args.workload, args.workload), "name": args.workload,
+                       "n_tokens": N, "pairs": plan.n_pairs, "hq": hq, "hkv": hkv, "d": d,
+                       "softmax_scale": scale, "l2": "flushed between timed steps (512 MB write, untimed)",
+                       "parallelism": f"replicas x{world} (independent trees per GPU)"},
+            "pct_peak": 100.0 * value / world / peak_burst,
+            "fwd_ms": fwd_ms, "bwd_pre_ms": pre_ms, "bwd_main_ms": main_ms, "bwd_post_ms": post_ms,
+            "fwd_tflops": f_fwd / (fwd_ms / 1e3) / 1e12, "bwd_main_tflops": f_bwd / (main_ms / 1e3) / 1e12,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk,
+            "speedup_vs_expanded": expanded["speedup"] if expanded else None,
+            "expanded": expanded,
+            "wall_s_timed_region": wall,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

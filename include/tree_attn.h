@@ -110,7 +110,9 @@ typedef struct {
     int32_t* kv_qhi;      /* [n_qtiles]                                         */
     int32_t* fwd_order;   /* [n_qtiles]    q-tiles, heaviest first              */
     int32_t* bwd_items;   /* [4*n_bwd_items] {kv-tile, q-tile begin, end,
-                                           partial slot or -1}, heaviest first  */
+                                           partial slot or -1}: q-ranges cut at
+                                           multiples of bwd_chunk_qtiles, run
+                                           chunk by chunk, longest first within */
 } tree_attn_plan_arrays_t;
 
 /* Build a plan from a rollout tree or forest (host only, no GPU needed).

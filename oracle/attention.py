@@ -85,7 +85,7 @@ def causal_backward(q, k, v, o, lse, do, scale: float):
     dq = np.zeros_like(q)
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)
-    delta = np.einsum("lhd,lhd->hl", do, o)                          # rowsum(dO * O)
+    delta = (do * o).sum(axis=2).T                                   # rowsum(dO * O), [Hq, L]
     rb = _rows_per_block(g, L)
     for hk in range(hkv):
         hs = slice(hk * g, (hk + 1) * g)
@@ -98,11 +98,13 @@ def causal_backward(q, k, v, o, lse, do, scale: float):
             rows = np.arange(r0, r1)[:, None]
             cols = np.arange(r1)[None, :]
             P = np.where(cols <= rows, np.exp(S - lse[hs, r0:r1, None]), 0.0)
-            dv[:r1, hk, :] += np.einsum("gic,gid->cd", P, dOg[:, r0:r1, :])
+            rows_g = g * (r1 - r0)
+            # sum over the group's heads and the block's rows: P^T dO
+            dv[:r1, hk, :] += P.transpose(2, 0, 1).reshape(r1, rows_g) @ dOg[:, r0:r1, :].reshape(rows_g, d)
             dP = dOg[:, r0:r1, :] @ Vh[:r1].T
             dS = P * (dP - delta[hs, r0:r1, None])
             dq[r0:r1, hs, :] = (scale * (dS @ Kh[:r1])).transpose(1, 0, 2)
-            dk[:r1, hk, :] += scale * np.einsum("gic,gid->cd", dS, Qg[:, r0:r1, :])
+            dk[:r1, hk, :] += scale * (dS.transpose(2, 0, 1).reshape(r1, rows_g) @ Qg[:, r0:r1, :].reshape(rows_g, d))
     return dq, dk, dv
 
 

@@ -41,15 +41,18 @@ EncodeTiledFn get_encode() {
     return fn;
 }
 
-// [rows, heads, d] bf16, boxes of 64 (d) x 1 (head) x 128 (rows), 128-byte swizzle.
-int make_tmap(CUtensorMap* m, const void* base, int64_t rows, int heads, int d) {
+// [rows, heads, d] bf16 (or fp32), boxes of 128 bytes of d x 1 head x 128 rows,
+// 128-byte swizzle.
+int make_tmap(CUtensorMap* m, const void* base, int64_t rows, int heads, int d, bool fp32 = false) {
     EncodeTiledFn enc = get_encode();
     if (!enc) return TREE_ATTN_ERR_CUDA;
+    const cuuint64_t es = fp32 ? 4 : 2;
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows};
-    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
-    cuuint32_t box[3] = {64, 1, kBlock};
+    cuuint64_t strides[2] = {(cuuint64_t)d * es, (cuuint64_t)heads * d * es};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / es), 1, kBlock};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+    CUresult r = enc(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                     const_cast<void*>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
@@ -297,12 +300,13 @@ int tree_attn_bwd_stages(tree_attn_plan_t P, const void* q, const void* k, const
     DevicePlan* D = nullptr;
     st = ensure_device(P, &D);
     if (st) return st;
-    CUtensorMap tq, tk, tv, tdo;
+    char* ws = static_cast<char*>(workspace);
+    CUtensorMap tq, tk, tv, tdo, tdq;
     if ((st = make_tmap(&tq, q, P->N, hq, d)) || (st = make_tmap(&tk, k, P->N, hkv, d)) ||
-        (st = make_tmap(&tv, v, P->N, hkv, d)) || (st = make_tmap(&tdo, dout, P->N, hq, d)))
+        (st = make_tmap(&tv, v, P->N, hkv, d)) || (st = make_tmap(&tdo, dout, P->N, hq, d)) ||
+        (st = make_tmap(&tdq, ws + w.dq_acc, P->N, hq, d, true)))
         return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    char* ws = static_cast<char*>(workspace);
     const int32_t Npad = P->T * kBlock;
 
     BwdPreParams pre;
@@ -345,7 +349,7 @@ int tree_attn_bwd_stages(tree_attn_plan_t P, const void* q, const void* k, const
     const int64_t n_items = (int64_t)P->bwd_items.size() / 4;
     if (n_items * hkv > INT32_MAX) return TREE_ATTN_ERR_TOO_LARGE;
     if (stages & TREE_ATTN_BWD_MAIN) {
-        e = launch_bwd(d, &tq, &tk, &tv, &tdo, p, (int)(n_items * hkv), s);
+        e = launch_bwd(d, &tq, &tk, &tv, &tdo, &tdq, p, (int)(n_items * hkv), s);
         if (e != cudaSuccess) return TREE_ATTN_ERR_CUDA;
     }
 

@@ -4,21 +4,29 @@
 // contiguous descendant q-range) x one kv-head.  The CTA keeps K_c and V_c in
 // shared memory and dV, dK in TMEM, and walks every step (q-tile t, q-head h
 // of the group) in a fixed order -- t ascending, then h ascending -- so dK and
-// dV are summed in the same order on every run.  Per step:
+// dV are summed in the same order on every run.  Per step n:
 //
-//   S^T  = K Q^T        (keys x queries, TMEM cols [0,128))
-//   dP^T = V dO^T       (TMEM cols [128,256))
-//   P^T  = exp2(S^T * scale*log2e - LSE*log2e)   masked: j <= i < subend[j]
-//   dS^T = P^T * (dP^T - Delta)                  (both written to smem, bf16)
-//   dV  += P^T dO       (TMEM cols [256, 256+D))
-//   dK  += dS^T Q       (TMEM cols [256+D, 256+2D))
-//   dQ   = dS K         (TMEM cols [0, D), reusing S^T), read out and added
-//                       to the fp32 dQ accumulator with vector reductions
+//   S^T  = K Q^T                TMEM cols [0,128)
+//   dP^T = V dO^T               TMEM cols [128,256)
+//   P^T  = exp2(S^T*scale*log2e - LSE*log2e), masked j <= i < subend[j];
+//          written back over S^T as packed bf16 (TMEM cols [0,64))
+//   dS^T = P^T * (dP^T - Delta) shared memory, bf16, K-major 128B-swizzled
+//          (P^T here is the bf16-rounded value that also feeds dV)
+//   dQ   = dS K                 TMEM cols [128,128+D) (over dP^T), issued first
+//   dK  += dS^T Q               TMEM cols [256+D, 256+2D)
+//   dV  += P^T dO               TMEM cols [256, 256+D), P^T read from TMEM
+//   S^T(n+1)                    issued right after, overlapping the dQ readout
+//   dP^T(n+1)                   once dQ(n) has left TMEM
 //
-// Warp roles (192 threads): warps 0-3 compute P^T / dS^T (one key row per
-// thread) and read dQ out (one query row per thread); warp 4 is the TMA
-// producer (K, V once; Q and dO per step through a ring; LSE and Delta rows by
-// bulk copy); warp 5 issues the MMAs and owns TMEM.
+// dQ leaves TMEM through registers into a 32 KB shared staging tile (fp32,
+// 128B-swizzled) and reaches the fp32 dQ accumulator by TMA bulk reduce-add,
+// 64 columns per round, while the tensor core runs dK and dV.
+//
+// Warp roles (320 threads): warps 0-7 compute (warp w owns TMEM lanes
+// 32*(w%4).. and query / dQ columns of half w/4); warp 8 is the TMA producer
+// (K, V once; Q and dO per step through a 3-slot ring, the next tiles
+// prefetched into L2; LSE and Delta rows by bulk copy); warp 9 issues the MMAs
+// and owns TMEM.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -29,28 +37,30 @@ namespace {
 template <int D>
 struct BwdCfg {
     static constexpr int TILE = 128 * D * 2;
-    static constexpr int PB = 128 * 128 * 2;
     static constexpr int NSLOT = D == 128 ? 3 : 4;
     static constexpr int SMALL = 3072;
     static constexpr int OFF_K = SMALL;
     static constexpr int OFF_V = OFF_K + TILE;
     static constexpr int OFF_RING = OFF_V + TILE;
-    static constexpr int OFF_PT = OFF_RING + NSLOT * TILE;
-    static constexpr int OFF_DST = OFF_PT + PB;
-    static constexpr int BYTES = OFF_DST + PB;
-    static constexpr int NWARPS = 6;
-    static constexpr int PRODUCER = 4;
-    static constexpr int MMA = 5;
+    static constexpr int OFF_DST = OFF_RING + NSLOT * TILE;   // dS^T, 128 x 128 bf16
+    static constexpr int OFF_STAGE = OFF_DST + 32768;         // dQ staging, 128 x 64 fp32
+    static constexpr int BYTES = OFF_STAGE + 32768;
+    static constexpr int NWARPS = 10;
+    static constexpr int NCOMPUTE = 256;                      // warps 0-7
+    static constexpr int PRODUCER = 8;
+    static constexpr int MMA = 9;
     static constexpr int TMEM_COLS = 512;
-    static constexpr int T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D, T_DQ = 0;
+    static constexpr int T_S = 0, T_P = 0, T_DP = 128, T_DQ = 128, T_DV = 256, T_DK = 256 + D;
+    static constexpr int ROUNDS = D / 64;                     // dQ staging rounds of 64 columns
     // small region
     static constexpr int B_KVFULL = 0;
-    static constexpr int B_FULL = 8;                     // [NSLOT]
-    static constexpr int B_EMPTY = B_FULL + 8 * NSLOT;   // [NSLOT]
-    static constexpr int B_LFULL = B_EMPTY + 8 * NSLOT;  // [2]
-    static constexpr int B_LEMPTY = B_LFULL + 16;        // [2]
+    static constexpr int B_FULL = 8;                      // [NSLOT]
+    static constexpr int B_EMPTY = B_FULL + 8 * NSLOT;    // [NSLOT]
+    static constexpr int B_LFULL = B_EMPTY + 8 * NSLOT;   // [2]
+    static constexpr int B_LEMPTY = B_LFULL + 16;         // [2]
     static constexpr int B_SFULL = B_LEMPTY + 16;
-    static constexpr int B_PFULL = B_SFULL + 8;
+    static constexpr int B_DPFULL = B_SFULL + 8;
+    static constexpr int B_PFULL = B_DPFULL + 8;
     static constexpr int B_DQFULL = B_PFULL + 8;
     static constexpr int B_DQEMPTY = B_DQFULL + 8;
     static constexpr int B_DKVFULL = B_DQEMPTY + 8;
@@ -66,7 +76,7 @@ template <int D>
 __global__ void __launch_bounds__(BwdCfg<D>::NWARPS * 32, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-               const BwdParams p) {
+               const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
     using C = BwdCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sb = smem_u32(smem);
@@ -91,12 +101,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::NWARPS * 32, 1)
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(C::B_LFULL + 8 * s), 1);
-            mbar_init(bar(C::B_LEMPTY + 8 * s), 128);
+            mbar_init(bar(C::B_LEMPTY + 8 * s), C::NCOMPUTE);
         }
         mbar_init(bar(C::B_SFULL), 1);
-        mbar_init(bar(C::B_PFULL), 128);
+        mbar_init(bar(C::B_DPFULL), 1);
+        mbar_init(bar(C::B_PFULL), C::NCOMPUTE);
         mbar_init(bar(C::B_DQFULL), 1);
-        mbar_init(bar(C::B_DQEMPTY), 128);
+        mbar_init(bar(C::B_DQEMPTY), C::NCOMPUTE);
         mbar_init(bar(C::B_DKVFULL), 1);
         mbar_init(bar(C::B_DRAIN), 1);
         fence_mbar_init();
@@ -107,6 +118,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::NWARPS * 32, 1)
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::HOLDER);
 
+    // ring position of step n's Q (w = 0) or dO (w = 1)
+    auto ring_pos = [](int n, int w) { return 2 * n + w; };
+
     if (warp == C::PRODUCER) {
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
@@ -116,11 +130,21 @@ __global__ void __launch_bounds__(BwdCfg<D>::NWARPS * 32, 1)
                 tma_load_3d(sb + C::OFF_K + blk * 16384, &tm_k, blk * 64, hk, c * 128, bar(C::B_KVFULL));
                 tma_load_3d(sb + C::OFF_V + blk * 16384, &tm_v, blk * 64, hk, c * 128, bar(C::B_KVFULL));
             }
+            auto prefetch = [&](int n) {
+                if (n >= nsteps) return;
+                const int t = t0 + n / G, h = hk * G + n % G;
+                for (int blk = 0; blk < D / 64; ++blk) {
+                    tma_prefetch_3d(&tm_q, blk * 64, h, t * 128);
+                    tma_prefetch_3d(&tm_do, blk * 64, h, t * 128);
+                }
+            };
+            prefetch(1);
             bool ok = true;
             for (int n = 0; n < nsteps && ok; ++n) {
                 const int t = t0 + n / G, h = hk * G + n % G;
+                prefetch(n + 2);
                 for (int w = 0; w < 2 && ok; ++w) {   // w = 0: Q, 1: dO
-                    const int pos = 2 * n + w, s = pos % C::NSLOT, use = pos / C::NSLOT;
+                    const int pos = ring_pos(n, w), s = pos % C::NSLOT, use = pos / C::NSLOT;
                     if (use > 0) ok = mbar_wait(bar(C::B_EMPTY + 8 * s), (use - 1) & 1, p.status, 21);
                     if (!ok) break;
                     mbar_expect_tx(bar(C::B_FULL + 8 * s), C::TILE);
@@ -142,58 +166,83 @@ __global__ void __launch_bounds__(BwdCfg<D>::NWARPS * 32, 1)
     } else if (warp == C::MMA) {
         if (lane == 0) {
             constexpr uint32_t ID_S = idesc_bf16(128, 128, false, false);   // K Q^T, V dO^T
-            constexpr uint32_t ID_KV = idesc_bf16(128, D, false, true);     // P^T dO, dS^T Q
-            constexpr uint32_t ID_Q = idesc_bf16(128, D, true, true);       // dS K
-            const uint32_t ka = sb + C::OFF_K, va = sb + C::OFF_V;
-            const uint32_t pta = sb + C::OFF_PT, dsa = sb + C::OFF_DST;
-            bool ok = mbar_wait(bar(C::B_KVFULL), 0, p.status, 23);
-            for (int n = 0; n < nsteps && ok; ++n) {
-                const int qpos = 2 * n, qs = qpos % C::NSLOT;
-                const int dpos = 2 * n + 1, ds = dpos % C::NSLOT;
-                ok = mbar_wait(bar(C::B_FULL + 8 * qs), (qpos / C::NSLOT) & 1, p.status, 24);
-                if (ok) ok = mbar_wait(bar(C::B_FULL + 8 * ds), (dpos / C::NSLOT) & 1, p.status, 25);
-                if (ok && n > 0) ok = mbar_wait(bar(C::B_DQEMPTY), (n - 1) & 1, p.status, 26);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t qa = sb + C::OFF_RING + qs * C::TILE, doa = sb + C::OFF_RING + ds * C::TILE;
+            constexpr uint32_t ID_DV = idesc_bf16(128, D, false, true);     // P^T (TMEM) dO
+            constexpr uint32_t ID_DK = idesc_bf16(128, D, false, true);     // dS^T Q
+            constexpr uint32_t ID_DQ = idesc_bf16(128, D, true, true);      // dS K
+            const uint32_t ka = sb + C::OFF_K, va = sb + C::OFF_V, dsa = sb + C::OFF_DST;
+            auto slot_of = [&](int n, int w) { return ring_pos(n, w) % C::NSLOT; };
+            auto wait_full = [&](int n, int w, int where) {
+                const int pos = ring_pos(n, w);
+                return mbar_wait(bar(C::B_FULL + 8 * (pos % C::NSLOT)), (pos / C::NSLOT) & 1, p.status, where);
+            };
+            auto issue_s = [&](int n) {   // S^T = K Q_n^T
+                const uint32_t qa = sb + C::OFF_RING + slot_of(n, 0) * C::TILE;
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-                    mma_bf16_ss(tmem + C::T_S, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024), ID_S,
-                                k > 0);
+                    mma_bf16_ss(tmem + C::T_S, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024),
+                                ID_S, k > 0);
                 }
+                mma_commit(bar(C::B_SFULL));
+            };
+            auto issue_dp = [&](int n) {   // dP^T = V dO_n^T
+                const uint32_t doa = sb + C::OFF_RING + slot_of(n, 1) * C::TILE;
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
                     mma_bf16_ss(tmem + C::T_DP, sdesc_sw128(va + off, 16, 1024), sdesc_sw128(doa + off, 16, 1024),
                                 ID_S, k > 0);
                 }
-                mma_commit(bar(C::B_SFULL));
+                mma_commit(bar(C::B_DPFULL));
+            };
+            bool ok = mbar_wait(bar(C::B_KVFULL), 0, p.status, 23);
+            if (ok) ok = wait_full(0, 0, 24);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0);
+                ok = wait_full(0, 1, 25);
+            }
+            if (ok) {
+                tc_fence_after();
+                issue_dp(0);
+            }
+            for (int n = 0; n < nsteps && ok; ++n) {
                 ok = mbar_wait(bar(C::B_PFULL), n & 1, p.status, 27);
                 if (!ok) break;
                 tc_fence_after();
-                // dV += P^T dO ; dK += dS^T Q   (K dimension = 128 queries)
+                const uint32_t qa = sb + C::OFF_RING + slot_of(n, 0) * C::TILE;
+                const uint32_t doa = sb + C::OFF_RING + slot_of(n, 1) * C::TILE;
+                // dQ = dS K   (M = queries: A is dS^T read MN-major; K dimension = 128 keys)
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint32_t aoff = (k >> 2) * 16384 + (k & 3) * 32;
-                    mma_bf16_ss(tmem + C::T_DV, sdesc_sw128(pta + aoff, 16, 1024),
-                                sdesc_sw128(doa + k * 2048, 16384, 1024), ID_KV, (n > 0 || k > 0) ? 1u : 0u);
-                }
+                for (int k = 0; k < 8; ++k)
+                    mma_bf16_ss(tmem + C::T_DQ, sdesc_sw128(dsa + k * 2048, 16384, 1024),
+                                sdesc_sw128(ka + k * 2048, 16384, 1024), ID_DQ, k > 0);
+                mma_commit(bar(C::B_DQFULL));
+                // dK += dS^T Q   (K dimension = 128 queries)
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const uint32_t aoff = (k >> 2) * 16384 + (k & 3) * 32;
                     mma_bf16_ss(tmem + C::T_DK, sdesc_sw128(dsa + aoff, 16, 1024),
-                                sdesc_sw128(qa + k * 2048, 16384, 1024), ID_KV, (n > 0 || k > 0) ? 1u : 0u);
+                                sdesc_sw128(qa + k * 2048, 16384, 1024), ID_DK, (n > 0 || k > 0) ? 1u : 0u);
                 }
-                // dQ = dS K   (M = queries, K dimension = 128 keys; both operands MN-major)
+                mma_commit(bar(C::B_EMPTY + 8 * slot_of(n, 0)));
+                // dV += P^T dO   (P^T from TMEM: 8 packed columns per 16 queries)
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    mma_bf16_ss(tmem + C::T_DQ, sdesc_sw128(dsa + k * 2048, 16384, 1024),
-                                sdesc_sw128(ka + k * 2048, 16384, 1024), ID_Q, k > 0);
+                for (int k = 0; k < 8; ++k)
+                    mma_bf16_ts(tmem + C::T_DV, tmem + C::T_P + k * 8, sdesc_sw128(doa + k * 2048, 16384, 1024),
+                                ID_DV, (n > 0 || k > 0) ? 1u : 0u);
+                mma_commit(bar(C::B_EMPTY + 8 * slot_of(n, 1)));
+                if (n + 1 < nsteps) {
+                    ok = wait_full(n + 1, 0, 24);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(n + 1);
+                    ok = wait_full(n + 1, 1, 25);
+                    if (ok) ok = mbar_wait(bar(C::B_DQEMPTY), n & 1, p.status, 26);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_dp(n + 1);
                 }
-                mma_commit(bar(C::B_DQFULL));
-                mma_commit(bar(C::B_EMPTY + 8 * qs));
-                mma_commit(bar(C::B_EMPTY + 8 * ds));
             }
             if (ok) mma_commit(bar(C::B_DKVFULL));
             mma_commit(bar(C::B_DRAIN));
@@ -202,87 +251,148 @@ __global__ void __launch_bounds__(BwdCfg<D>::NWARPS * 32, 1)
         __syncwarp();
     } else {
         // --------------------- P^T / dS^T, then dQ readout ---------------------
-        const int r = (warp << 5) + lane;            // TMEM lane
-        const uint32_t lane_base = tmem + ((uint32_t)(warp << 5) << 16);
-        const int j = c * 128 + r;                   // this thread's key
-        const int sub_j = p.subend[j];               // 0 past N
+        const int quarter = warp & 3, half = warp >> 2;
+        const int r = (quarter << 5) + lane;          // TMEM lane
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter << 5) << 16);
+        const int j = c * 128 + r;                    // this thread's key
+        const int sub_j = p.subend[j];                // 0 past N
         const float sl2 = p.scale_log2;
-        const uint32_t pta = sb + C::OFF_PT, dsa = sb + C::OFF_DST;
+        const uint32_t dsa = sb + C::OFF_DST;
+        const uint32_t stage = sb + C::OFF_STAGE;
         bool ok = true;
-        for (int n = 0; n < nsteps && ok; ++n) {
+        // After a failed wait the loop keeps running with the work skipped, so all
+        // compute threads meet the named barriers of every step.
+        for (int n = 0; n < nsteps; ++n) {
             const int t = t0 + n / G, h = hk * G + n % G;
             const int q0 = t * 128;
             const int lo = max(j - q0, 0), hi = min(sub_j - q0, 128);
             const int ls = n & 1;
-            ok = mbar_wait(bar(C::B_LFULL + 8 * ls), (n >> 1) & 1, p.status, 29);
+            if (ok) ok = mbar_wait(bar(C::B_LFULL + 8 * ls), (n >> 1) & 1, p.status, 29);
             if (ok) ok = mbar_wait(bar(C::B_SFULL), n & 1, p.status, 30);
-            if (!ok) break;
-            tc_fence_after();
+            ok = __all_sync(0xffffffffu, ok);
             const float4* lse4 = reinterpret_cast<const float4*>(smem + C::LSD + ls * 1024);
             const float4* del4 = reinterpret_cast<const float4*>(smem + C::LSD + ls * 1024 + 512);
+            // P^T for this thread's 64 query columns, kept in registers as the packed
+            // bf16 pairs that also feed the dV MMA (dS below uses the same values)
+            uint32_t pw[2][16];
+            if (ok) {
+                tc_fence_after();
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                float sv[32], dp[32];
-                tmem_ld32(lane_base + C::T_S + cc * 32, sv);
-                tmem_ld32(lane_base + C::T_DP + cc * 32, dp);
-                tmem_wait_ld();
-                uint32_t pw[16], dw[16];
+                for (int cq = 0; cq < 2; ++cq) {
+                    const int cc = half * 2 + cq;
+                    float sv[32];
+                    tmem_ld32(lane_base + C::T_S + cc * 32, sv);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int u4 = 0; u4 < 8; ++u4) {
-                    const float4 l4 = lse4[cc * 8 + u4];
-                    const float4 d4 = del4[cc * 8 + u4];
-                    const float la[4] = {l4.x, l4.y, l4.z, l4.w};
-                    const float da[4] = {d4.x, d4.y, d4.z, d4.w};
-                    float pv[4], dv[4];
+                    for (int u4 = 0; u4 < 8; ++u4) {
+                        const float4 l4 = lse4[cc * 8 + u4];
+                        const float la[4] = {l4.x, l4.y, l4.z, l4.w};
+                        float pe[4];
 #pragma unroll
-                    for (int w = 0; w < 4; ++w) {
-                        const int u = u4 * 4 + w;
-                        const int col = cc * 32 + u;
-                        float pe = fast_exp2(fmaf(sv[u], sl2, -la[w]));
-                        pe = (col >= lo && col < hi) ? pe : 0.f;
-                        pv[w] = pe;
-                        dv[w] = pe * (dp[u] - da[w]);
+                        for (int w = 0; w < 4; ++w) {
+                            const int u = u4 * 4 + w, col = cc * 32 + u;
+                            const float e = fast_exp2(fmaf(sv[u], sl2, -la[w]));
+                            pe[w] = (col >= lo && col < hi) ? e : 0.f;
+                        }
+                        pw[cq][u4 * 2] = pack_bf16x2(pe[0], pe[1]);
+                        pw[cq][u4 * 2 + 1] = pack_bf16x2(pe[2], pe[3]);
                     }
-                    pw[u4 * 2] = pack_bf16x2(pv[0], pv[1]);
-                    pw[u4 * 2 + 1] = pack_bf16x2(pv[2], pv[3]);
-                    dw[u4 * 2] = pack_bf16x2(dv[0], dv[1]);
-                    dw[u4 * 2 + 1] = pack_bf16x2(dv[2], dv[3]);
                 }
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    const int col = cc * 32 + g * 8;
-                    const uint32_t off = (col >> 6) * 16384 + sw128_offset(r, (col & 63) >> 3);
-                    st_shared_v4(pta + off, pw[4 * g], pw[4 * g + 1], pw[4 * g + 2], pw[4 * g + 3]);
-                    st_shared_v4(dsa + off, dw[4 * g], dw[4 * g + 1], dw[4 * g + 2], dw[4 * g + 3]);
-                }
+                tc_fence_before();
             }
-            mbar_arrive(bar(C::B_LEMPTY + 8 * ls));
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(bar(C::B_PFULL));
-            // dQ rows: this thread's TMEM lane is now query q0 + r
-            ok = mbar_wait(bar(C::B_DQFULL), n & 1, p.status, 31);
-            if (!ok) break;
-            tc_fence_after();
-            const int i = q0 + r;
-            float* dst = p.dq_acc + ((size_t)i * p.hq + h) * D;
+            // every thread has read its S^T columns before P^T overwrites them
+            ok = named_bar_and(1, C::NCOMPUTE, ok);
+            if (ok) {
+                tc_fence_after();
 #pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
-                float v[32];
-                tmem_ld32(lane_base + C::T_DQ + cc * 32, v);
-                tmem_wait_ld();
-                if (i < p.N) {
-#pragma unroll
-                    for (int u = 0; u < 32; u += 4)
-                        red_add_v4(dst + cc * 32 + u, v[u] * p.scale, v[u + 1] * p.scale, v[u + 2] * p.scale,
-                                   v[u + 3] * p.scale);
-                }
+                for (int cq = 0; cq < 2; ++cq) tmem_st16(lane_base + C::T_P + (half * 2 + cq) * 16, pw[cq]);
+                ok = mbar_wait(bar(C::B_DPFULL), n & 1, p.status, 33);
             }
-            tc_fence_before();
-            mbar_arrive(bar(C::B_DQEMPTY));
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok) {
+                tc_fence_after();
+#pragma unroll
+                for (int cq = 0; cq < 2; ++cq) {
+                    const int cc = half * 2 + cq;
+                    float dp[32];
+                    tmem_ld32(lane_base + C::T_DP + cc * 32, dp);
+                    tmem_wait_ld();
+                    uint32_t dw[16];
+#pragma unroll
+                    for (int u4 = 0; u4 < 8; ++u4) {
+                        const float4 d4 = del4[cc * 8 + u4];
+                        const float da[4] = {d4.x, d4.y, d4.z, d4.w};
+                        const float pv[4] = {__uint_as_float(pw[cq][u4 * 2] << 16),
+                                             __uint_as_float(pw[cq][u4 * 2] & 0xffff0000u),
+                                             __uint_as_float(pw[cq][u4 * 2 + 1] << 16),
+                                             __uint_as_float(pw[cq][u4 * 2 + 1] & 0xffff0000u)};
+                        float dv[4];
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) dv[w] = pv[w] * (dp[u4 * 4 + w] - da[w]);
+                        dw[u4 * 2] = pack_bf16x2(dv[0], dv[1]);
+                        dw[u4 * 2 + 1] = pack_bf16x2(dv[2], dv[3]);
+                    }
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        const int col = cc * 32 + g * 8;
+                        st_shared_v4(dsa + (col >> 6) * 16384 + sw128_offset(r, (col & 63) >> 3), dw[4 * g],
+                                     dw[4 * g + 1], dw[4 * g + 2], dw[4 * g + 3]);
+                    }
+                }
+                mbar_arrive(bar(C::B_LEMPTY + 8 * ls));
+                tmem_wait_st();
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(bar(C::B_PFULL));
+                ok = mbar_wait(bar(C::B_DQFULL), n & 1, p.status, 31);
+            }
+            ok = __all_sync(0xffffffffu, ok);
+            // dQ rows: this thread's TMEM lane is now query q0 + r, columns of its half
+            float qv[D / 2];
+            if (ok) {
+                tc_fence_after();
+#pragma unroll
+                for (int cq = 0; cq < D / 64; ++cq) {
+                    float v[32];
+                    tmem_ld32(lane_base + C::T_DQ + (half * (D / 64) + cq) * 32, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) qv[cq * 32 + u] = v[u] * p.scale;
+                }
+                tc_fence_before();
+                mbar_arrive(bar(C::B_DQEMPTY));   // dQ has left TMEM
+            }
+            // staging rounds of 64 columns: round k holds the columns of half k
+            // (D = 128) or both halves (D = 64)
+#pragma unroll
+            for (int rd = 0; rd < C::ROUNDS; ++rd) {
+                if (ok && (C::ROUNDS == 1 || half == rd)) {
+#pragma unroll
+                    for (int cq = 0; cq < D / 64; ++cq) {
+                        const int blk = C::ROUNDS == 1 ? half : cq;   // 32-column block inside the staging tile
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            st_shared_v4(stage + blk * 16384 + sw128_offset(r, k), __float_as_uint(qv[cq * 32 + 4 * k]),
+                                         __float_as_uint(qv[cq * 32 + 4 * k + 1]),
+                                         __float_as_uint(qv[cq * 32 + 4 * k + 2]),
+                                         __float_as_uint(qv[cq * 32 + 4 * k + 3]));
+                    }
+                }
+                fence_proxy_async_smem();
+                ok = named_bar_and(1, C::NCOMPUTE, ok);
+                if (ok && threadIdx.x == 0) {
+                    for (int blk = 0; blk < 2; ++blk)
+                        tma_reduce_add_3d(&tm_dq, stage + blk * 16384, rd * 64 + blk * 32, h, q0);
+                    bulk_commit();
+                    bulk_wait_read_all();   // the staging tile may be written again
+                }
+                if (rd + 1 < C::ROUNDS) named_bar_sync(1, C::NCOMPUTE);
+            }
         }
+        if (threadIdx.x == 0) bulk_wait_all();
         // ------------------------------ dK, dV ---------------------------------
         if (ok) ok = mbar_wait(bar(C::B_DKVFULL), 0, p.status, 32);
+        ok = __all_sync(0xffffffffu, ok);
         if (ok) {
             tc_fence_after();
             for (int which = 0; which < 2; ++which) {   // 0: dK, 1: dV
@@ -291,7 +401,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::NWARPS * 32, 1)
                 if (slot < 0) {
                     uint16_t* out = (which == 0 ? p.dk : p.dv) + ((size_t)j * p.hkv + hk) * D;
 #pragma unroll
-                    for (int cc = 0; cc < D / 32; ++cc) {
+                    for (int cc = half * (D / 64); cc < (half + 1) * (D / 64); ++cc) {
                         float v[32];
                         tmem_ld32(lane_base + tcol + cc * 32, v);
                         tmem_wait_ld();
@@ -310,7 +420,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::NWARPS * 32, 1)
                 } else {
                     float* out = p.part + ((((size_t)slot * p.hkv + hk) * 2 + which) * 128 + r) * D;
 #pragma unroll
-                    for (int cc = 0; cc < D / 32; ++cc) {
+                    for (int cc = half * (D / 64); cc < (half + 1) * (D / 64); ++cc) {
                         float v[32];
                         tmem_ld32(lane_base + tcol + cc * 32, v);
                         tmem_wait_ld();
@@ -333,22 +443,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::NWARPS * 32, 1)
 
 template <int D>
 cudaError_t launch_cfg(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv, const CUtensorMap* tdo,
-                       const BwdParams& p, int grid, cudaStream_t stream) {
+                       const CUtensorMap* tdq, const BwdParams& p, int grid, cudaStream_t stream) {
     using C = BwdCfg<D>;
     auto kern = bwd_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES);
     if (e != cudaSuccess) return e;
-    kern<<<grid, C::NWARPS * 32, C::BYTES, stream>>>(*tq, *tk, *tv, *tdo, p);
+    kern<<<grid, C::NWARPS * 32, C::BYTES, stream>>>(*tq, *tk, *tv, *tdo, *tdq, p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_bwd(int d, const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
-                       const CUtensorMap* tdo, const BwdParams& p, int grid, cudaStream_t stream) {
+                       const CUtensorMap* tdo, const CUtensorMap* tdq, const BwdParams& p, int grid,
+                       cudaStream_t stream) {
     if (grid <= 0) return cudaSuccess;
-    return d == 128 ? launch_cfg<128>(tq, tk, tv, tdo, p, grid, stream)
-                    : launch_cfg<64>(tq, tk, tv, tdo, p, grid, stream);
+    return d == 128 ? launch_cfg<128>(tq, tk, tv, tdo, tdq, p, grid, stream)
+                    : launch_cfg<64>(tq, tk, tv, tdo, tdq, p, grid, stream);
 }
 
 }  // namespace treeattn

@@ -214,14 +214,17 @@ __global__ void __launch_bounds__(FwdCfg<D, NS>::NWARPS * 32, 1)
             const bool partial = ent & 1;
             int my_sub = 0;
             if (partial) my_sub = p.subend[c * 128 + r];
-            ok = mbar_wait(b_sfull(s), j & 1, p.status, 8);
-            if (!ok) break;
-            tc_fence_after();
+            // After a failed wait the loop keeps running (work skipped) so that every
+            // thread of the group meets the same named barriers in the same order.
+            if (ok) ok = mbar_wait(b_sfull(s), j & 1, p.status, 8);
+            ok = __all_sync(0xffffffffu, ok);
             if (partial) {
-                named_bar_sync(1 + s, 128);
-                sub_sm[r] = my_sub;
+                ok = named_bar_and(1 + s, 128, ok);
+                if (ok) sub_sm[r] = my_sub;
                 named_bar_sync(1 + s, 128);
             }
+            if (!ok) continue;
+            tc_fence_after();
             // pass 1: row maximum (scaled, masked) over the 128 key columns
             const int kbase = c * 128;
             auto masked_scaled = [&](float (&v)[32], int cc) {
@@ -302,6 +305,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NS>::NWARPS * 32, 1)
         }
         // ------------------------------ epilogue -----------------------------
         if (ok) ok = mbar_wait(b_ofull(s), 0, p.status, 9);
+        ok = named_bar_and(1 + s, 128, ok);
         if (ok) {
             tc_fence_after();
             const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;

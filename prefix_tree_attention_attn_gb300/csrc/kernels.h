@@ -59,7 +59,8 @@ cudaError_t launch_fwd(int d, int nstream, const CUtensorMap* tq, const CUtensor
                        const CUtensorMap* to, const FwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t stream);
 cudaError_t launch_bwd(int d, const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
-                       const CUtensorMap* tdo, const BwdParams& p, int grid, cudaStream_t stream);
+                       const CUtensorMap* tdo, const CUtensorMap* tdq, const BwdParams& p, int grid,
+                       cudaStream_t stream);
 cudaError_t launch_bwd_post(const BwdPostParams& p, cudaStream_t stream);
 
 }  // namespace treeattn

@@ -216,31 +216,36 @@ int build_plan(const int32_t* parent, const int32_t* seg_len, int32_t n, const t
             return P->qt_ptr[x + 1] - P->qt_ptr[x] > P->qt_ptr[y + 1] - P->qt_ptr[y];
         });
 
-        // backward schedule: each kv-tile's q-range, cut into near-equal chunks
+        // backward schedule: each kv-tile's q-range [c, kv_qhi) cut at the global
+        // multiples of S, so that the items of every kv-tile that feed the same
+        // q-tiles share one chunk index; items run chunk by chunk (then longest
+        // first), which keeps the dQ rows they accumulate into resident in L2.
         const int64_t entries = (int64_t)P->qt_kv.size();
         int32_t S = chunk_opt > 0 ? chunk_opt : (int32_t)std::max<int64_t>(8, ceil_div(entries, 1216));
         P->chunk = S;
-        std::vector<int32_t> items;
+        std::vector<int32_t> items;   // {c, t0, t1, slot} plus a sort key below
+        std::vector<int32_t> chunk_of;
         for (int32_t c = 0; c < T; ++c) {
             const int32_t lo = P->kv_qlo[c], hi = P->kv_qhi[c];
-            const int32_t L = hi - lo;
-            const int32_t nc = (int32_t)ceil_div(L, S);
+            const int32_t k0 = lo / S, k1 = (hi - 1) / S;
+            const int32_t nc = k1 - k0 + 1;
             int32_t base = -1;
             if (nc > 1) {
                 base = (int32_t)P->n_slots;
                 P->splits.insert(P->splits.end(), {c, base, nc, 0});
                 P->n_slots += nc;
             }
-            for (int32_t k = 0; k < nc; ++k) {
-                const int32_t t0 = lo + (int32_t)((int64_t)L * k / nc);
-                const int32_t t1 = lo + (int32_t)((int64_t)L * (k + 1) / nc);
-                items.insert(items.end(), {c, t0, t1, nc > 1 ? base + k : -1});
+            for (int32_t k = k0; k <= k1; ++k) {
+                const int32_t t0 = std::max(lo, k * S), t1 = std::min(hi, (k + 1) * S);
+                items.insert(items.end(), {c, t0, t1, nc > 1 ? base + (k - k0) : -1});
+                chunk_of.push_back(k);
             }
         }
         const int32_t n_items = (int32_t)(items.size() / 4);
         std::vector<int32_t> idx(n_items);
         for (int32_t i = 0; i < n_items; ++i) idx[i] = i;
         std::stable_sort(idx.begin(), idx.end(), [&](int32_t x, int32_t y) {
+            if (chunk_of[x] != chunk_of[y]) return chunk_of[x] < chunk_of[y];
             return items[4 * x + 2] - items[4 * x + 1] > items[4 * y + 2] - items[4 * y + 1];
         });
         P->bwd_items.resize(items.size());

@@ -56,7 +56,6 @@ def check_schedules(p, e):
     slots = set()
     for c, t0, t1, slot in items.tolist():
         assert e["kv_qlo"][c] <= t0 < t1 <= e["kv_qhi"][c]
-        assert t1 - t0 <= S
         covered.setdefault(c, []).append((t0, t1))
         if slot >= 0:
             assert slot not in slots
@@ -66,8 +65,10 @@ def check_schedules(p, e):
         segs = sorted(covered[c])
         assert segs[0][0] == e["kv_qlo"][c] and segs[-1][1] == e["kv_qhi"][c]
         assert all(segs[k][1] == segs[k + 1][0] for k in range(len(segs) - 1))
-    lens = items[:, 2] - items[:, 1]
-    assert all(lens[k] >= lens[k + 1] for k in range(len(lens) - 1))
+    # q-ranges are cut at multiples of S; items run chunk by chunk, longest first within
+    assert all((t0 // S) == ((t1 - 1) // S) for _, t0, t1, _ in items.tolist())
+    keys = [(t0 // S, -(t1 - t0)) for _, t0, t1, _ in items.tolist()]
+    assert keys == sorted(keys)
 
 
 def test_golden_tiny_tree():

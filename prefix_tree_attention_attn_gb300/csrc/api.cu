@@ -43,13 +43,14 @@ EncodeTiledFn get_encode() {
 
 // [rows, heads, d] bf16 (or fp32), boxes of 128 bytes of d x 1 head x 128 rows,
 // 128-byte swizzle.
-int make_tmap(CUtensorMap* m, const void* base, int64_t rows, int heads, int d, bool fp32 = false) {
+int make_tmap(CUtensorMap* m, const void* base, int64_t rows, int heads, int d, bool fp32 = false,
+              int box_rows = kBlock) {
     EncodeTiledFn enc = get_encode();
     if (!enc) return TREE_ATTN_ERR_CUDA;
     const cuuint64_t es = fp32 ? 4 : 2;
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows};
     cuuint64_t strides[2] = {(cuuint64_t)d * es, (cuuint64_t)heads * d * es};
-    cuuint32_t box[3] = {(cuuint32_t)(128 / es), 1, kBlock};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / es), 1, (cuuint32_t)box_rows};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                      const_cast<void*>(base), dims, strides, box, estr,
@@ -349,7 +350,17 @@ int tree_attn_bwd_stages(tree_attn_plan_t P, const void* q, const void* k, const
     const int64_t n_items = (int64_t)P->bwd_items.size() / 4;
     if (n_items * hkv > INT32_MAX) return TREE_ATTN_ERR_TOO_LARGE;
     if (stages & TREE_ATTN_BWD_MAIN) {
-        e = launch_bwd(d, &tq, &tk, &tv, &tdo, &tdq, p, (int)(n_items * hkv), s);
+        if (d == 128) {
+            // 64-row boxes: Q / dO half tiles and dQ^T half tiles of the ping-pong kernel
+            CUtensorMap tq64, tdo64, tdq64;
+            if ((st = make_tmap(&tq64, q, P->N, hq, d, false, 64)) ||
+                (st = make_tmap(&tdo64, dout, P->N, hq, d, false, 64)) ||
+                (st = make_tmap(&tdq64, ws + w.dq_acc, P->N, hq, d, true, 64)))
+                return st;
+            e = launch_bwd_pp(&tq, &tk, &tv, &tdo, &tdq64, &tq64, &tdo64, p, (int)(n_items * hkv), s);
+        } else {
+            e = launch_bwd(d, &tq, &tk, &tv, &tdo, &tdq, p, (int)(n_items * hkv), s);
+        }
         if (e != cudaSuccess) return TREE_ATTN_ERR_CUDA;
     }
 

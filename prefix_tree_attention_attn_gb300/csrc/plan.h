@@ -6,7 +6,7 @@
 #include <mutex>
 #include <vector>
 
-#include "../../include/tree_attn.h"
+#include "tree_attn.h"
 
 namespace treeattn {
 

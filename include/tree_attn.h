@@ -63,6 +63,8 @@ extern "C" {
 #define TREE_ATTN_ERR_NO_DEVICE       -8  /* no usable sm_103 device              */
 #define TREE_ATTN_ERR_OUT_OF_MEMORY   -9  /* host or device allocation failed     */
 #define TREE_ATTN_ERR_DEVICE_TIMEOUT -10  /* a bounded device wait ran out        */
+#define TREE_ATTN_ERR_SCRATCH_TOO_SMALL -11 /* tree_attn_bwd_noalloc: the problem
+                                             needs more than its fixed scratch    */
 
 /* ---- tile classes (tree_attn_plan_export) ------------------------------- */
 #define TREE_ATTN_TILE_FULL     1   /* every valid (query, key) pair attended  */
@@ -168,6 +170,35 @@ int tree_attn_bwd_stages(tree_attn_plan_t plan, const void* q, const void* k, co
                          void* dq, void* dk, void* dv, int32_t hq, int32_t hkv, int32_t d,
                          float softmax_scale, void* workspace, size_t ws_bytes, void* stream,
                          int32_t stages);
+
+/* Backward that allocates nothing.  (The pages have no counterpart: this is a
+ * convenience of this library.)  Some callers cannot call cudaMalloc or
+ * cudaFree at the point where they run the backward: code whose device memory
+ * is owned by another allocator (a framework's caching pool that has claimed
+ * the memory), code that must not synchronise the device (cudaMalloc and
+ * cudaFree can), or code held to a fixed memory budget.  This entry point takes
+ * the same tensors as tree_attn_bwd but no workspace: the plan's tables and the
+ * workspace go into one fixed array in device memory that the library declares
+ * at file scope, tree_attn_noalloc_scratch_bytes() bytes (32 MiB), held by every
+ * device that loads the library until the process exits.
+ *  - Problems whose tables plus workspace exceed that size are rejected with
+ *    TREE_ATTN_ERR_SCRATCH_TOO_SMALL (use tree_attn_bwd with a workspace).
+ *  - Every call uses the same array.  Calls that run at the same time on the
+ *    GPU (different streams, or different host threads) race on it; serialise
+ *    them, e.g. on one stream.  Each call overwrites the array before reading
+ *    it, so nothing from an earlier call leaks into the result.
+ *  - The first call on a device looks up the array's device address.  The call
+ *    copies the plan tables from host memory (a short synchronous staging of a
+ *    few kilobytes) and calls no cudaMalloc, cudaFree or allocating routine.
+ * Arguments, layouts, stream semantics and the other status codes are those of
+ * tree_attn_bwd. */
+int tree_attn_bwd_noalloc(tree_attn_plan_t plan, const void* q, const void* k, const void* v,
+                          const void* o, const float* lse, const void* dout,
+                          void* dq, void* dk, void* dv, int32_t hq, int32_t hkv, int32_t d,
+                          float softmax_scale, void* stream);
+
+/* Size in bytes of the fixed scratch tree_attn_bwd_noalloc uses. */
+size_t tree_attn_noalloc_scratch_bytes(void);
 
 /* Synchronise `stream`, then read and clear the device status word of the
  * current device: 0 when every kernel's bounded waits finished in time,

@@ -167,6 +167,34 @@ def tree_attn_bwd(plan: TreePlan, q, k, v, o, lse, dout, softmax_scale: float, d
     return dq, dk, dv
 
 
+def tree_attn_bwd_noalloc(plan: TreePlan, q, k, v, o, lse, dout, softmax_scale: float, dq, dk, dv, stream=None):
+    """Backward into caller-provided dq / dk / dv without allocating anything
+    (``tree_attn_bwd_noalloc``): for callers that cannot allocate device memory
+    at this point, because another allocator owns it, because allocation could
+    synchronise the device, or because of a fixed memory budget.  The library's
+    fixed scratch (``noalloc_scratch_bytes()``) bounds the problem size, and
+    calls that overlap on the GPU share that scratch, so run them one after
+    another."""
+    import torch
+    N, hq, d = q.shape
+    hkv = k.shape[1]
+    for name, t, shp, dt in (("q", q, (N, hq, d), torch.bfloat16), ("k", k, (N, hkv, d), torch.bfloat16),
+                             ("v", v, (N, hkv, d), torch.bfloat16), ("o", o, (N, hq, d), torch.bfloat16),
+                             ("lse", lse, (hq, N), torch.float32), ("dout", dout, (N, hq, d), torch.bfloat16),
+                             ("dq", dq, (N, hq, d), torch.bfloat16), ("dk", dk, (N, hkv, d), torch.bfloat16),
+                             ("dv", dv, (N, hkv, d), torch.bfloat16)):
+        _check_tensor(t, name, shp, dt)
+    B.check(B.load().tree_attn_bwd_noalloc(plan.handle, _dptr(q), _dptr(k), _dptr(v), _dptr(o), _dptr(lse),
+                                           _dptr(dout), _dptr(dq), _dptr(dk), _dptr(dv), hq, hkv, d,
+                                           float(softmax_scale), _stream_ptr(stream)), "tree_attn_bwd_noalloc")
+    return dq, dk, dv
+
+
+def noalloc_scratch_bytes() -> int:
+    """Bytes of the fixed device scratch that ``tree_attn_bwd_noalloc`` uses."""
+    return int(B.load().tree_attn_noalloc_scratch_bytes())
+
+
 def device_status(stream=None) -> int:
     """Synchronise and read/clear the kernels' device status word (0 = fine)."""
     return int(B.load().tree_attn_get_device_status(_stream_ptr(stream)))

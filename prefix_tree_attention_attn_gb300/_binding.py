@@ -47,6 +47,10 @@ SIGNATURES = {
     "tree_attn_bwd_stages": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                        C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32, C.c_int32,
                                        C.c_int32, C.c_float, C.c_void_p, C.c_size_t, C.c_void_p, C.c_int32]),
+    "tree_attn_bwd_noalloc": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                        C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32, C.c_int32,
+                                        C.c_int32, C.c_float, C.c_void_p]),
+    "tree_attn_noalloc_scratch_bytes": (C.c_size_t, []),
     "tree_attn_get_device_status": (C.c_int, [C.c_void_p]),
     "tree_attn_plan_destroy": (None, [C.c_void_p]),
     "tree_attn_strerror": (C.c_char_p, [C.c_int]),

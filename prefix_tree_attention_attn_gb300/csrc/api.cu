@@ -380,6 +380,154 @@ int tree_attn_bwd_stages(tree_attn_plan_t P, const void* q, const void* k, const
     return e == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
 }
 
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Backward without any allocation: the scratch lives in a fixed device array.
+// ---------------------------------------------------------------------------
+
+namespace treeattn {
+namespace {
+
+// One shared scratch array per device that loads this library; it holds the
+// plan's device tables and the backward workspace of one call at a time.
+constexpr size_t kNoAllocScratchBytes = 32u << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device (with that device current); host code must not use the symbol
+// itself as a device pointer.
+int noalloc_scratch_ptr(int dev, unsigned char** out) {
+    static unsigned char* ptrs[kMaxDevices] = {};
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!ptrs[dev]) {
+        void* a = nullptr;
+        if (cudaGetSymbolAddress(&a, g_noalloc_scratch) != cudaSuccess) return TREE_ATTN_ERR_CUDA;
+        ptrs[dev] = static_cast<unsigned char*>(a);
+    }
+    *out = ptrs[dev];
+    return TREE_ATTN_OK;
+}
+
+}  // namespace
+}  // namespace treeattn
+
+extern "C" {
+
+int tree_attn_bwd_noalloc(tree_attn_plan_t P, const void* q, const void* k, const void* v, const void* o,
+                          const float* lse, const void* dout, void* dq, void* dk, void* dv, int32_t hq,
+                          int32_t hkv, int32_t d, float softmax_scale, void* stream) {
+    if (!P || !q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return TREE_ATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(softmax_scale)) return TREE_ATTN_ERR_INVALID_ARG;
+    int st = check_heads(P, hq, hkv, d);
+    if (st) return st;
+    for (const void* ptr : {q, k, v, o, (const void*)lse, dout, (const void*)dq, (const void*)dk, (const void*)dv})
+        if (!aligned16(ptr)) return TREE_ATTN_ERR_ALIGNMENT;
+    int dev = 0;
+    if ((st = current_device(&dev))) return st;
+
+    // plan tables (the same layout the uploaded plan uses), then the workspace
+    const int64_t T = P->T;
+    const int64_t n_ent = (int64_t)P->qt_kv.size();
+    const int64_t n_items = (int64_t)P->bwd_items.size() / 4;
+    const int64_t n_splits = (int64_t)P->splits.size() / 4;
+    const int64_t sizes[5] = {T * kBlock, T, 4 * n_items, 4 * std::max<int64_t>(n_splits, 1), 0};
+    int64_t offs[5], words = 0;
+    for (int i = 0; i < 5; ++i) {
+        offs[i] = words;
+        words += (sizes[i] + 63) / 64 * 64;
+    }
+    const size_t table_bytes = (size_t)words * sizeof(int32_t);
+    const WsLayout w = bwd_layout(P, hq, hkv, d);
+    if (table_bytes + w.total > kNoAllocScratchBytes) return TREE_ATTN_ERR_SCRATCH_TOO_SMALL;
+    if (n_items * hkv > INT32_MAX) return TREE_ATTN_ERR_TOO_LARGE;
+
+    unsigned char* scratch = nullptr;
+    if ((st = noalloc_scratch_ptr(dev, &scratch))) return st;
+    int* status = nullptr;
+    if ((st = status_ptr(dev, &status))) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    std::vector<int32_t> h((size_t)words, 0);
+    std::copy(P->subend.begin(), P->subend.end(), h.begin() + offs[0]);
+    std::copy(P->kv_minsub.begin(), P->kv_minsub.end(), h.begin() + offs[1]);
+    std::copy(P->bwd_items.begin(), P->bwd_items.end(), h.begin() + offs[2]);
+    std::copy(P->splits.begin(), P->splits.end(), h.begin() + offs[3]);
+    // pageable source: the copy is staged before the call returns
+    if (cudaMemcpyAsync(scratch, h.data(), table_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return TREE_ATTN_ERR_CUDA;
+    const int32_t* tab = reinterpret_cast<const int32_t*>(scratch);
+    char* ws = reinterpret_cast<char*>(scratch) + table_bytes;   // 256-byte aligned
+
+    CUtensorMap tq, tk, tv, tdo, tdq;
+    if ((st = make_tmap(&tq, q, P->N, hq, d)) || (st = make_tmap(&tk, k, P->N, hkv, d)) ||
+        (st = make_tmap(&tv, v, P->N, hkv, d)) || (st = make_tmap(&tdo, dout, P->N, hq, d)) ||
+        (st = make_tmap(&tdq, ws + w.dq_acc, P->N, hq, d, true)))
+        return st;
+    const int32_t Npad = P->T * kBlock;
+
+    BwdPreParams pre;
+    pre.o = static_cast<const uint16_t*>(o);
+    pre.dout = static_cast<const uint16_t*>(dout);
+    pre.lse = lse;
+    pre.delta = reinterpret_cast<float*>(ws + w.delta);
+    pre.lse2 = reinterpret_cast<float*>(ws + w.lse2);
+    pre.dq_acc = reinterpret_cast<float*>(ws + w.dq_acc);   // zeroed by the pre kernel
+    pre.N = (int32_t)P->N;
+    pre.Npad = Npad;
+    pre.hq = hq;
+    pre.d = d;
+    if (launch_bwd_pre(pre, s) != cudaSuccess) return TREE_ATTN_ERR_CUDA;
+
+    BwdParams p;
+    p.items = tab + offs[2];
+    p.subend = tab + offs[0];
+    p.kv_minsub = tab + offs[1];
+    p.delta = pre.delta;
+    p.lse2 = pre.lse2;
+    p.dq_acc = pre.dq_acc;
+    p.dk = static_cast<uint16_t*>(dk);
+    p.dv = static_cast<uint16_t*>(dv);
+    p.part = reinterpret_cast<float*>(ws + w.part);
+    p.N = (int32_t)P->N;
+    p.Npad = Npad;
+    p.hq = hq;
+    p.hkv = hkv;
+    p.group = hq / hkv;
+    p.scale = softmax_scale;
+    p.scale_log2 = softmax_scale * 1.4426950408889634f;
+    p.status = status;
+    cudaError_t e;
+    if (d == 128) {
+        CUtensorMap tq64, tdo64, tdq64;
+        if ((st = make_tmap(&tq64, q, P->N, hq, d, false, 64)) ||
+            (st = make_tmap(&tdo64, dout, P->N, hq, d, false, 64)) ||
+            (st = make_tmap(&tdq64, ws + w.dq_acc, P->N, hq, d, true, 64)))
+            return st;
+        e = launch_bwd_pp(&tq, &tk, &tv, &tdo, &tdq64, &tq64, &tdo64, p, (int)(n_items * hkv), s);
+    } else {
+        e = launch_bwd(d, &tq, &tk, &tv, &tdo, &tdq, p, (int)(n_items * hkv), s);
+    }
+    if (e != cudaSuccess) return TREE_ATTN_ERR_CUDA;
+
+    BwdPostParams post;
+    post.dq_acc = pre.dq_acc;
+    post.dq = static_cast<uint16_t*>(dq);
+    post.splits = tab + offs[3];
+    post.part = p.part;
+    post.dk = p.dk;
+    post.dv = p.dv;
+    post.N = (int32_t)P->N;
+    post.hq = hq;
+    post.hkv = hkv;
+    post.d = d;
+    post.n_splits = (int32_t)n_splits;
+    return launch_bwd_post(post, s) == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
+}
+
+size_t tree_attn_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
+
 int tree_attn_get_device_status(void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return TREE_ATTN_ERR_CUDA;
     int v = 0, zero = 0;
@@ -413,6 +561,9 @@ const char* tree_attn_strerror(int s) {
         case TREE_ATTN_ERR_CUDA: return "CUDA runtime or driver error";
         case TREE_ATTN_ERR_NO_DEVICE: return "no usable sm_103 device";
         case TREE_ATTN_ERR_OUT_OF_MEMORY: return "out of memory";
+        case TREE_ATTN_ERR_SCRATCH_TOO_SMALL:
+            return "problem too large for the fixed scratch of tree_attn_bwd_noalloc "
+                   "(see tree_attn_noalloc_scratch_bytes)";
         default:
             if (s <= TREE_ATTN_ERR_DEVICE_TIMEOUT) return "a bounded device wait ran out";
             return "unknown status";

@@ -30,7 +30,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_status_codes_named(lib):
     text = open(HEADER).read()
     codes = {int(v) for v in re.findall(r"#define TREE_ATTN_(?:OK|ERR_[A-Z_]+)\s+(-?\d+)", text)}
-    assert codes == set(range(-10, 1))
+    assert codes == set(range(-11, 1))
     for code in codes:
         s = lib.tree_attn_strerror(code).decode()
         assert s and s != "unknown status"

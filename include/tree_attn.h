@@ -138,8 +138,8 @@ int tree_attn_plan_upload(tree_attn_plan_t plan);
 int tree_attn_workspace_size(tree_attn_plan_t plan, int32_t hq, int32_t hkv, int32_t d,
                              size_t* fwd_bytes, size_t* bwd_bytes);
 
-/* Forward: O and LSE (see the formulas above).  softmax_scale is applied to
- * the logits (pass 1/sqrt(d) for standard attention).  d in {64, 128}.  The
+/* Forward: O and LSE (see the formulas above).  softmax_scale (> 0, finite)
+ * is applied to the logits (pass 1/sqrt(d) for standard attention).  d in {64, 128}.  The
  * forward needs no workspace (pass NULL, 0).  Work is queued on `stream`. */
 int tree_attn_fwd(tree_attn_plan_t plan, const void* q, const void* k, const void* v,
                   void* o, float* lse, int32_t hq, int32_t hkv, int32_t d,

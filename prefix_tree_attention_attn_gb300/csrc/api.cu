@@ -245,7 +245,7 @@ int tree_attn_fwd(tree_attn_plan_t P, const void* q, const void* k, const void* 
     (void)workspace;
     (void)ws_bytes;
     if (!P || !q || !k || !v || !o || !lse) return TREE_ATTN_ERR_INVALID_ARG;
-    if (!std::isfinite(softmax_scale)) return TREE_ATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f)) return TREE_ATTN_ERR_INVALID_ARG;
     int st = check_heads(P, hq, hkv, d);
     if (st) return st;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
@@ -290,7 +290,7 @@ int tree_attn_bwd_stages(tree_attn_plan_t P, const void* q, const void* k, const
                          int32_t stages) {
     if (stages <= 0 || stages > 7) return TREE_ATTN_ERR_INVALID_ARG;
     if (!P || !q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return TREE_ATTN_ERR_INVALID_ARG;
-    if (!std::isfinite(softmax_scale)) return TREE_ATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f)) return TREE_ATTN_ERR_INVALID_ARG;
     int st = check_heads(P, hq, hkv, d);
     if (st) return st;
     for (const void* ptr : {q, k, v, o, (const void*)lse, dout, (const void*)dq, (const void*)dk, (const void*)dv})
@@ -419,7 +419,7 @@ int tree_attn_bwd_noalloc(tree_attn_plan_t P, const void* q, const void* k, cons
                           const float* lse, const void* dout, void* dq, void* dk, void* dv, int32_t hq,
                           int32_t hkv, int32_t d, float softmax_scale, void* stream) {
     if (!P || !q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return TREE_ATTN_ERR_INVALID_ARG;
-    if (!std::isfinite(softmax_scale)) return TREE_ATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f)) return TREE_ATTN_ERR_INVALID_ARG;
     int st = check_heads(P, hq, hkv, d);
     if (st) return st;
     for (const void* ptr : {q, k, v, o, (const void*)lse, dout, (const void*)dq, (const void*)dk, (const void*)dv})

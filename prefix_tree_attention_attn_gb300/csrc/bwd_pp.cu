@@ -269,26 +269,37 @@ __global__ void __launch_bounds__(PpCfg::NWARPS * 32, 1)
                 const int cbase = 64 * x + 32 * ch;     // this thread's first query column in the step
                 if (ok) ok = mbar_wait(bar(C::B_SDP + 8 * x), n & 1, p.status, 50);
                 ok = __all_sync(0xffffffffu, ok);
-                uint32_t pw[16];
+                float pk[32];      // P^T for this thread's 32 query columns (fp32, for dS)
+                uint32_t pw[16];   // the same, packed bf16 (for TMEM and the dV MMA)
                 if (ok) {
                     tc_fence_after();
                     float sv[32];
                     tmem_ld32(lane_base + 128 * x + 32 * ch, sv);
                     tmem_wait_ld();
+                    if (lo <= cbase && hi >= cbase + 32) {   // every column of this row attends
 #pragma unroll
-                    for (int u4 = 0; u4 < 8; ++u4) {
-                        const float4 l4 = lse4[cbase / 4 + u4];
-                        const float la[4] = {l4.x, l4.y, l4.z, l4.w};
-                        float pe[4];
-#pragma unroll
-                        for (int w = 0; w < 4; ++w) {
-                            const int col = cbase + u4 * 4 + w;
-                            const float e = fast_exp2(fmaf(sv[u4 * 4 + w], sl2, -la[w]));
-                            pe[w] = (col >= lo && col < hi) ? e : 0.f;
+                        for (int u4 = 0; u4 < 8; ++u4) {
+                            const float4 l4 = lse4[cbase / 4 + u4];
+                            pk[u4 * 4 + 0] = fast_exp2(fmaf(sv[u4 * 4 + 0], sl2, -l4.x));
+                            pk[u4 * 4 + 1] = fast_exp2(fmaf(sv[u4 * 4 + 1], sl2, -l4.y));
+                            pk[u4 * 4 + 2] = fast_exp2(fmaf(sv[u4 * 4 + 2], sl2, -l4.z));
+                            pk[u4 * 4 + 3] = fast_exp2(fmaf(sv[u4 * 4 + 3], sl2, -l4.w));
                         }
-                        pw[u4 * 2] = pack_bf16x2(pe[0], pe[1]);
-                        pw[u4 * 2 + 1] = pack_bf16x2(pe[2], pe[3]);
+                    } else {
+#pragma unroll
+                        for (int u4 = 0; u4 < 8; ++u4) {
+                            const float4 l4 = lse4[cbase / 4 + u4];
+                            const float la[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                            for (int w = 0; w < 4; ++w) {
+                                const int col = cbase + u4 * 4 + w;
+                                const float e = fast_exp2(fmaf(sv[u4 * 4 + w], sl2, -la[w]));
+                                pk[u4 * 4 + w] = (col >= lo && col < hi) ? e : 0.f;
+                            }
+                        }
                     }
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) pw[u] = pack_bf16x2(pk[2 * u], pk[2 * u + 1]);
                     tc_fence_before();
                 }
                 // every thread has read its S^T_x columns before P^T_x overwrites them,
@@ -306,13 +317,9 @@ __global__ void __launch_bounds__(PpCfg::NWARPS * 32, 1)
                     for (int u4 = 0; u4 < 8; ++u4) {
                         const float4 d4 = del4[cbase / 4 + u4];
                         const float da[4] = {d4.x, d4.y, d4.z, d4.w};
-                        const float pv[4] = {__uint_as_float(pw[u4 * 2] << 16),
-                                             __uint_as_float(pw[u4 * 2] & 0xffff0000u),
-                                             __uint_as_float(pw[u4 * 2 + 1] << 16),
-                                             __uint_as_float(pw[u4 * 2 + 1] & 0xffff0000u)};
                         float dv[4];
 #pragma unroll
-                        for (int w = 0; w < 4; ++w) dv[w] = pv[w] * (dp[u4 * 4 + w] - da[w]);
+                        for (int w = 0; w < 4; ++w) dv[w] = pk[u4 * 4 + w] * (dp[u4 * 4 + w] - da[w]);
                         dw[u4 * 2] = pack_bf16x2(dv[0], dv[1]);
                         dw[u4 * 2 + 1] = pack_bf16x2(dv[2], dv[3]);
                     }

@@ -16,8 +16,12 @@
 //
 // Pipeline on the tensor core:  S0(0) S1(0) | PV0(0) S0(1) | PV1(0) S1(1) | ...
 // While softmax group 0 turns S0(j) into P0(j), the tensor core runs q-head 1's
-// MMAs, and the other way round.  P goes to shared memory (bf16, swizzled as a
-// K-major operand) and feeds O += P V.  O is rescaled in TMEM only when a
+// MMAs, and the other way round.  P is written back over S in TMEM (packed
+// bf16) and feeds O += P V as the A operand, so it never touches shared
+// memory (whose bandwidth the MMAs' operand reads already use up).  The
+// softmax is bound by its FMA/ALU instructions, so pass 1 takes the maximum of
+// the raw logits (the scale is positive) and pass 2 is one FFMA into ex2 per
+// element.  O is rescaled in TMEM only when a
 // row's running maximum grows by more than 2^8 (the accumulated sum and O keep
 // one common reference maximum, so the result is unchanged).
 //
@@ -33,13 +37,12 @@ namespace {
 template <int D, int NS>
 struct FwdCfg {
     static constexpr int TILE = 128 * D * 2;          // Q/K/V tile bytes
-    static constexpr int PB = 128 * 128 * 2;          // P tile bytes
-    static constexpr int NSLOT = (D == 128 && NS == 2) ? 3 : 4;
     static constexpr int SMALL = 3072;                // barriers + subend staging
+    // K/V ring: every slot that fits next to Q (at most 8)
+    static constexpr int NSLOT = (229376 - NS * TILE) / TILE < 8 ? (229376 - NS * TILE) / TILE : 8;
     static constexpr int OFF_Q = SMALL;
     static constexpr int OFF_KV = OFF_Q + NS * TILE;
-    static constexpr int OFF_P = OFF_KV + NSLOT * TILE;
-    static constexpr int BYTES = OFF_P + NS * PB;
+    static constexpr int BYTES = OFF_KV + NSLOT * TILE;
     static constexpr int NWARPS = 4 * NS + 2;
     static constexpr int PRODUCER = 4 * NS;
     static constexpr int MMA = 4 * NS + 1;
@@ -57,6 +60,7 @@ struct FwdCfg {
     static_assert(SUB + NS * 512 <= SMALL, "small region");
     static_assert(HOLDER + 4 <= SUB, "barriers");
     static_assert(BYTES <= 232448, "shared memory");
+    static_assert(NSLOT >= NS && NSLOT >= 3, "the epilogue stages O in ring slots");
 };
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
@@ -147,14 +151,12 @@ __global__ void __launch_bounds__(FwdCfg<D, NS>::NWARPS * 32, 1)
                                 IDESC_S, k > 0);
                 }
             };
-            auto issue_pv = [&](int s, int slot, bool acc) {
-                const uint32_t pa = sb + C::OFF_P + s * C::PB, va = sb + C::OFF_KV + slot * C::TILE;
+            auto issue_pv = [&](int s, int slot, bool acc) {   // O += P V, P from TMEM
+                const uint32_t va = sb + C::OFF_KV + slot * C::TILE;
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint32_t aoff = (k >> 2) * 16384 + (k & 3) * 32;
-                    mma_bf16_ss(tmem + s * 256 + 128, sdesc_sw128(pa + aoff, 16, 1024),
-                                sdesc_sw128(va + k * 2048, 16384, 1024), IDESC_PV, (acc || k > 0) ? 1u : 0u);
-                }
+                for (int k = 0; k < 8; ++k)
+                    mma_bf16_ts(tmem + s * 256 + 128, tmem + s * 256 + k * 8, sdesc_sw128(va + k * 2048, 16384, 1024),
+                                IDESC_PV, (acc || k > 0) ? 1u : 0u);
             };
             bool ok = mbar_wait(b_qfull, 0, p.status, 2);
             if (ok) ok = mbar_wait(b_kvfull(0), 0, p.status, 3);
@@ -176,7 +178,10 @@ __global__ void __launch_bounds__(FwdCfg<D, NS>::NWARPS * 32, 1)
                     tc_fence_after();
                     issue_pv(s, vslot, j > 0);
                     if (s == NS - 1) mma_commit(b_kvempty(vslot));
-                    if (j == n_kv - 1) mma_commit(b_ofull(s));
+                    // O is final for every head once the last head's last PV is done;
+                    // only then may the epilogue reuse ring slots for staging
+                    if (j == n_kv - 1 && s == NS - 1)
+                        for (int ss = 0; ss < NS; ++ss) mma_commit(b_ofull(ss));
                     if (j + 1 < n_kv) {
                         const int kpos = 2 * (j + 1), kslot = kpos % C::NSLOT;
                         if (s == 0) {
@@ -204,7 +209,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NS>::NWARPS * 32, 1)
         const uint32_t tS = lane_base + s * 256;
         const uint32_t tO = tS + 128;
         int32_t* sub_sm = reinterpret_cast<int32_t*>(smem + C::SUB + s * 512);
-        const uint32_t p_base = sb + C::OFF_P + s * C::PB;
+        const uint32_t o_stage = sb + C::OFF_KV + s * C::TILE;   // ring slot s, idle once O is final
         const float sl2 = p.scale_log2;
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
@@ -225,36 +230,32 @@ __global__ void __launch_bounds__(FwdCfg<D, NS>::NWARPS * 32, 1)
             }
             if (!ok) continue;
             tc_fence_after();
-            // pass 1: row maximum (scaled, masked) over the 128 key columns
+            // pass 1: row maximum of the raw logits (masked) over the 128 key columns
             const int kbase = c * 128;
-            auto masked_scaled = [&](float (&v)[32], int cc) {
-                if (partial) {
+            auto mask = [&](float (&v)[32], int cc) {
 #pragma unroll
-                    for (int u4 = 0; u4 < 8; ++u4) {
-                        const int4 sv = reinterpret_cast<const int4*>(sub_sm)[cc * 8 + u4];
-                        const int sa[4] = {sv.x, sv.y, sv.z, sv.w};
+                for (int u4 = 0; u4 < 8; ++u4) {
+                    const int4 sv = reinterpret_cast<const int4*>(sub_sm)[cc * 8 + u4];
+                    const int sa[4] = {sv.x, sv.y, sv.z, sv.w};
 #pragma unroll
-                        for (int w = 0; w < 4; ++w) {
-                            const int u = u4 * 4 + w;
-                            const bool keep = (kbase + cc * 32 + u <= i) && (i < sa[w]);
-                            v[u] = keep ? v[u] * sl2 : -INFINITY;
-                        }
+                    for (int w = 0; w < 4; ++w) {
+                        const int u = u4 * 4 + w;
+                        const bool keep = (kbase + cc * 32 + u <= i) && (i < sa[w]);
+                        v[u] = keep ? v[u] : -INFINITY;
                     }
-                } else {
-#pragma unroll
-                    for (int u = 0; u < 32; ++u) v[u] *= sl2;
                 }
             };
-            float mx = -INFINITY;
+            float mraw = -INFINITY;
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 float v[32];
                 tmem_ld32(tS + cc * 32, v);
                 tmem_wait_ld();
-                masked_scaled(v, cc);
+                if (partial) mask(v, cc);
 #pragma unroll
-                for (int u = 0; u < 32; ++u) mx = fmaxf(mx, v[u]);
+                for (int u = 0; u < 32; ++u) mraw = fmaxf(mraw, v[u]);
             }
+            const float mx = mraw * sl2;   // softmax_scale > 0, so the maximum commutes with it
             const float m_new = fmaxf(m_run, mx);
             const bool need = m_new > m_run + kRescaleThreshold;   // false while both are -inf
             const float factor = need ? fast_exp2(m_run - m_new) : 1.f;
@@ -275,31 +276,27 @@ __global__ void __launch_bounds__(FwdCfg<D, NS>::NWARPS * 32, 1)
                 m_run = m_new;
             }
             const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-            // pass 2: P = 2^(x - m) -> bf16 -> shared memory (K-major, swizzled)
+            // pass 2: P = 2^(s * scale*log2e - m) -> packed bf16 over S's first 64
+            // columns (each store lands on columns this thread has already read)
             float lsum = 0.f;
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 float v[32];
                 tmem_ld32(tS + cc * 32, v);
                 tmem_wait_ld();
-                masked_scaled(v, cc);
+                if (partial) mask(v, cc);
+                uint32_t pw[16];
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    uint32_t w4[4];
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        const float a = fast_exp2(v[g * 8 + 2 * h] - m_use);
-                        const float b = fast_exp2(v[g * 8 + 2 * h + 1] - m_use);
-                        lsum += a + b;
-                        w4[h] = pack_bf16x2(a, b);
-                    }
-                    const int col = cc * 32 + g * 8;
-                    st_shared_v4(p_base + (col >> 6) * 16384 + sw128_offset(r, (col & 63) >> 3), w4[0], w4[1],
-                                 w4[2], w4[3]);
+                for (int h = 0; h < 16; ++h) {
+                    const float a = fast_exp2(fmaf(v[2 * h], sl2, -m_use));
+                    const float b = fast_exp2(fmaf(v[2 * h + 1], sl2, -m_use));
+                    lsum += a + b;
+                    pw[h] = pack_bf16x2(a, b);
                 }
+                tmem_st16(tS + cc * 16, pw);
             }
             l_run += lsum;
-            fence_proxy_async_smem();
+            tmem_wait_st();
             tc_fence_before();
             mbar_arrive(b_pfull(s));
         }
@@ -309,7 +306,8 @@ __global__ void __launch_bounds__(FwdCfg<D, NS>::NWARPS * 32, 1)
         if (ok) {
             tc_fence_after();
             const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-            // O (bf16) into this head's P buffer, laid out like a TMA tile of Q
+            // O (bf16) into ring slot s (every load has been consumed by then),
+            // laid out like a TMA tile of Q
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) {
                 float v[32];
@@ -318,7 +316,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NS>::NWARPS * 32, 1)
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
                     const int col = cc * 32 + g * 8;   // first of 8 columns
-                    st_shared_v4(p_base + (col >> 6) * 16384 + sw128_offset(r, (col & 63) >> 3),
+                    st_shared_v4(o_stage + (col >> 6) * 16384 + sw128_offset(r, (col & 63) >> 3),
                                  pack_bf16x2(v[g * 8 + 0] * inv_l, v[g * 8 + 1] * inv_l),
                                  pack_bf16x2(v[g * 8 + 2] * inv_l, v[g * 8 + 3] * inv_l),
                                  pack_bf16x2(v[g * 8 + 4] * inv_l, v[g * 8 + 5] * inv_l),
@@ -329,7 +327,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NS>::NWARPS * 32, 1)
             fence_proxy_async_smem();
             named_bar_sync(1 + s, 128);
             if (r == 0) {
-                for (int blk = 0; blk < D / 64; ++blk) tma_store_3d(&tm_o, p_base + blk * 16384, blk * 64, h0 + s, q0);
+                for (int blk = 0; blk < D / 64; ++blk) tma_store_3d(&tm_o, o_stage + blk * 16384, blk * 64, h0 + s, q0);
                 bulk_commit();
                 bulk_wait_all();
             }

@@ -94,6 +94,9 @@ def test_compute_calls_validate_before_touching_the_device(lib):
     assert lib.tree_attn_fwd(p.handle, odd, fake, fake, fake, fake, 2, 2, 64, 1.0, None, 0, None) == -5
     assert lib.tree_attn_fwd(p.handle, fake, fake, fake, fake, fake, 2, 2, 64, float("nan"),
                              None, 0, None) == -1
+    assert lib.tree_attn_fwd(p.handle, fake, fake, fake, fake, fake, 2, 2, 64, -0.5, None, 0, None) == -1
+    assert lib.tree_attn_bwd(p.handle, fake, fake, fake, fake, fake, fake, fake, fake, fake,
+                             2, 2, 64, 0.0, fake, 1 << 30, None) == -1
     # workspace too small
     assert lib.tree_attn_bwd(p.handle, fake, fake, fake, fake, fake, fake, fake, fake, fake,
                              2, 2, 64, 1.0, fake, 16, None) == -6

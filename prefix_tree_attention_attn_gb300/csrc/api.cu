@@ -264,6 +264,7 @@ int tree_attn_fwd(tree_attn_plan_t P, const void* q, const void* k, const void* 
     p.qt_ent = D->qt_ent;
     p.fwd_order = D->fwd_order;
     p.subend = D->subend;
+    p.kv_minsub = D->kv_minsub;
     p.lse = lse;
     p.N = (int32_t)P->N;
     p.hq = hq;

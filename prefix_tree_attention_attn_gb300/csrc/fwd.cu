@@ -26,7 +26,9 @@
 // one common reference maximum, so the result is unchanged).
 //
 // Masking: a full block needs none; a partial block keeps key j for row i iff
-// j <= i and i < subend[j] (the packed-layout lemma; see plan.cpp).
+// j <= i and i < subend[j] (the packed-layout lemma; see plan.cpp).  Inside a
+// partial block, a warp whose 32 rows all satisfy j_max <= i < min subend
+// needs no mask either.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -230,8 +232,13 @@ __global__ void __launch_bounds__(FwdCfg<D, NS>::NWARPS * 32, 1)
             }
             if (!ok) continue;
             tc_fence_after();
-            // pass 1: row maximum of the raw logits (masked) over the 128 key columns
+            // pass 1: row maximum of the raw logits over the 128 key columns.  A warp
+            // whose rows all see every key of the tile (j_max <= i < min subend) skips
+            // the mask; otherwise masked logits are set to -inf and written back to
+            // TMEM, so pass 2 never masks.
             const int kbase = c * 128;
+            const bool need_mask =
+                partial && !__all_sync(0xffffffffu, kbase + 127 <= i && i < p.kv_minsub[c]);
             auto mask = [&](float (&v)[32], int cc) {
 #pragma unroll
                 for (int u4 = 0; u4 < 8; ++u4) {
@@ -251,10 +258,14 @@ __global__ void __launch_bounds__(FwdCfg<D, NS>::NWARPS * 32, 1)
                 float v[32];
                 tmem_ld32(tS + cc * 32, v);
                 tmem_wait_ld();
-                if (partial) mask(v, cc);
+                if (need_mask) {
+                    mask(v, cc);
+                    tmem_st32(tS + cc * 32, v);
+                }
 #pragma unroll
                 for (int u = 0; u < 32; ++u) mraw = fmaxf(mraw, v[u]);
             }
+            if (need_mask) tmem_wait_st();
             const float mx = mraw * sl2;   // softmax_scale > 0, so the maximum commutes with it
             const float m_new = fmaxf(m_run, mx);
             const bool need = m_new > m_run + kRescaleThreshold;   // false while both are -inf
@@ -284,7 +295,6 @@ __global__ void __launch_bounds__(FwdCfg<D, NS>::NWARPS * 32, 1)
                 float v[32];
                 tmem_ld32(tS + cc * 32, v);
                 tmem_wait_ld();
-                if (partial) mask(v, cc);
                 uint32_t pw[16];
 #pragma unroll
                 for (int h = 0; h < 16; ++h) {

@@ -12,6 +12,7 @@ struct FwdParams {
     const int32_t* qt_ent;     // kv_tile*2 + partial
     const int32_t* fwd_order;  // [T]
     const int32_t* subend;     // [T*128], 0 past N
+    const int32_t* kv_minsub;  // [T] min subend over each kv-tile's keys
     float* lse;                // [hq, N]
     int32_t N, hq, group;
     float scale_log2;          // softmax_scale * log2(e)

@@ -312,9 +312,11 @@ def run_ours(args):
     post_ms = statistics.mean(p[3] for p in per)
 
     peak_burst, peak_sus, peak_src = measured_peaks()
-    dominant = ("bwd_kernel", main_ms, f_bwd) if main_ms >= fwd_ms else ("fwd_kernel", fwd_ms, f_fwd)
+    # the backward's tensor-core kernel is bwd_pp_kernel (bwd_pp.cu) for d = 128, bwd_kernel (bwd.cu) else
+    bwd_name, bwd_src = ("bwd_pp_kernel", "bwd_pp.cu") if d == 128 else ("bwd_kernel", "bwd.cu")
+    dominant = (bwd_name, main_ms, f_bwd, bwd_src) if main_ms >= fwd_ms else ("fwd_kernel", fwd_ms, f_fwd, "fwd.cu")
     achieved = dominant[2] / (dominant[1] / 1e3) / 1e12
-    src_hash = kernel_source_hash(["bwd.cu" if dominant[0] == "bwd_kernel" else "fwd.cu", "ptx.cuh"])
+    src_hash = kernel_source_hash([dominant[3], "ptx.cuh"])
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_burst, "unit": "TFLOP/s",
                 "frac": achieved / peak_burst, "traffic": recorded_traffic(dominant[0], args.workload, src_hash),
                 "kernel": dominant[0], "peak_source": f"{peak_src} bf16 burst",

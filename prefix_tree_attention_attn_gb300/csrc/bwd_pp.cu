@@ -22,12 +22,14 @@
 // (128B-swizzled), and reaches the accumulator by TMA bulk reduce-add.  The
 // reduce runs asynchronously; the staging tile is reused one half-step later.
 //
-// Warp roles (320 threads): warps 0-7 compute (warp w owns TMEM lanes
-// 32*(w%4).. -- keys for S^T / dP^T, features for dQ^T -- and 32 of the 64
-// query columns of a half: [32*(w/4), +32)); warp 8 is the TMA producer (K, V
-// once; Q and dO per half-step, 64 rows each, through a 6-slot ring so that
-// each half releases its own slots; the next tiles prefetched into L2; LSE and
-// Delta rows by bulk copy); warp 9 issues the MMAs and owns TMEM.
+// Warp roles (448 threads): warps 0-7 compute P^T and dS^T (warp w owns TMEM
+// lanes 32*(w%4).. -- one key each -- and 32 of the 64 query columns of a
+// half: [32*(w/4), +32)); warps 8-11 read dQ^T out of TMEM (lane = feature, all
+// 64 query columns) into the staging tile and issue the TMA reduce, so the
+// compute warps never wait for dQ; warp 12 is the TMA producer (K, V once; Q
+// and dO per half-step, 64 rows each, through a 6-slot ring so that each half
+// releases its own slots; the next tiles prefetched into L2; LSE and Delta rows
+// by bulk copy); warp 13 issues the MMAs and owns TMEM.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -47,10 +49,12 @@ struct PpCfg {
     static constexpr int OFF_DST = OFF_RING + NSLOT * HTILE;  // dS^T: 128 keys x 128 queries bf16 (2 blocks)
     static constexpr int OFF_STAGE = OFF_DST + 32768;         // dQ staging: 64 queries x 128 features fp32
     static constexpr int BYTES = OFF_STAGE + 32768;
-    static constexpr int NWARPS = 10;
-    static constexpr int NCOMPUTE = 256;
-    static constexpr int PRODUCER = 8;
-    static constexpr int MMA = 9;
+    static constexpr int NWARPS = 14;
+    static constexpr int NCOMPUTE = 256;                      // warps 0-7
+    static constexpr int READOUT0 = 8;                        // warps 8-11
+    static constexpr int NREADOUT = 128;
+    static constexpr int PRODUCER = 12;
+    static constexpr int MMA = 13;
     static constexpr int TMEM_COLS = 512;
     static constexpr int T_DV = 256, T_DK = 384;
     // small region
@@ -106,7 +110,7 @@ __global__ void __launch_bounds__(PpCfg::NWARPS * 32, 1)
             mbar_init(bar(C::B_SDP + 8 * s), 1);
             mbar_init(bar(C::B_PFULL + 8 * s), C::NCOMPUTE);
             mbar_init(bar(C::B_DQFULL + 8 * s), 1);
-            mbar_init(bar(C::B_DQEMPTY + 8 * s), C::NCOMPUTE);
+            mbar_init(bar(C::B_DQEMPTY + 8 * s), C::NREADOUT);
         }
         mbar_init(bar(C::B_DKVFULL), 1);
         mbar_init(bar(C::B_DRAIN), 1);
@@ -244,6 +248,50 @@ __global__ void __launch_bounds__(PpCfg::NWARPS * 32, 1)
             mbar_wait(bar(C::B_DRAIN), 0, p.status, 48);
         }
         __syncwarp();
+    } else if (warp >= C::READOUT0) {
+        // ------------------------------ dQ readout ------------------------------
+        const int quarter = warp & 3;
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter << 5) << 16);   // lane = feature
+        const uint32_t stage = sb + C::OFF_STAGE;
+        const int rtid = threadIdx.x - C::READOUT0 * 32;                        // 0..127
+        bool ok = true;
+        // loops run to the end after a failed wait (work skipped), so the named
+        // barriers of this warpgroup always line up
+        for (int n = 0; n < nsteps; ++n) {
+            const int t = t0 + n / G, h = hk * G + n % G;
+            const int q0 = t * 128;
+            for (int x = 0; x < 2; ++x) {
+                if (ok) ok = mbar_wait(bar(C::B_DQFULL + 8 * x), n & 1, p.status, 51);
+                ok = __all_sync(0xffffffffu, ok);
+                float v[64];
+                if (ok) {
+                    tc_fence_after();
+                    tmem_ld32(lane_base + 128 * x + 64, *reinterpret_cast<float(*)[32]>(&v[0]));
+                    tmem_ld32(lane_base + 128 * x + 96, *reinterpret_cast<float(*)[32]>(&v[32]));
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    mbar_arrive(bar(C::B_DQEMPTY + 8 * x));   // dQ^T_x has left TMEM
+                }
+                // the previous reduce has finished reading the staging tile
+                if (rtid == 0) bulk_wait_read_all();
+                ok = named_bar_and(2, C::NREADOUT, ok);
+                if (ok) {
+                    // staging [64 queries][128 features] fp32: 4 blocks of 32 features x 64 rows
+                    const uint32_t blk = stage + (uint32_t)quarter * 8192 + ((lane & 3) << 2);
+#pragma unroll
+                    for (int u = 0; u < 64; ++u)
+                        st_shared_f32(blk + u * 128 + ((((uint32_t)lane >> 2) ^ ((uint32_t)u & 7u)) << 4),
+                                      v[u] * p.scale);
+                }
+                fence_proxy_async_smem();
+                ok = named_bar_and(2, C::NREADOUT, ok);
+                if (ok && rtid == 0) {
+                    for (int b = 0; b < 4; ++b) tma_reduce_add_3d(&tm_dq64, stage + b * 8192, b * 32, h, q0 + 64 * x);
+                    bulk_commit();
+                }
+            }
+        }
+        if (rtid == 0) bulk_wait_all();
     } else {
         // ------------------------------ compute -------------------------------
         const int quarter = warp & 3, ch = warp >> 2;  // TMEM lane quarter, column half of a half-step
@@ -253,7 +301,6 @@ __global__ void __launch_bounds__(PpCfg::NWARPS * 32, 1)
         const int sub_j = p.subend[j];                 // 0 past N
         const float sl2 = p.scale_log2;
         const uint32_t dsa = sb + C::OFF_DST;
-        const uint32_t stage = sb + C::OFF_STAGE;
         bool ok = true;
         // After a failed wait the loops keep running with the work skipped, so all
         // compute threads meet the named barriers of every half-step.
@@ -302,9 +349,7 @@ __global__ void __launch_bounds__(PpCfg::NWARPS * 32, 1)
                     for (int u = 0; u < 16; ++u) pw[u] = pack_bf16x2(pk[2 * u], pk[2 * u + 1]);
                     tc_fence_before();
                 }
-                // every thread has read its S^T_x columns before P^T_x overwrites them,
-                // and the previous half-step's dQ staging has been read by TMA
-                if (threadIdx.x == 0) bulk_wait_read_all();
+                // every thread has read its S^T_x columns before P^T_x overwrites them
                 ok = named_bar_and(1, C::NCOMPUTE, ok);
                 if (ok) {
                     tc_fence_after();
@@ -333,35 +378,9 @@ __global__ void __launch_bounds__(PpCfg::NWARPS * 32, 1)
                     fence_proxy_async_smem();
                     tc_fence_before();
                     mbar_arrive(bar(C::B_PFULL + 8 * x));
-                    ok = mbar_wait(bar(C::B_DQFULL + 8 * x), n & 1, p.status, 51);
-                }
-                ok = __all_sync(0xffffffffu, ok);
-                if (ok) {
-                    // dQ^T_x: lane r = feature r; columns = this thread's 32 queries
-                    tc_fence_after();
-                    float v[32];
-                    tmem_ld32(lane_base + 128 * x + 64 + 32 * ch, v);
-                    tmem_wait_ld();
-                    tc_fence_before();
-                    mbar_arrive(bar(C::B_DQEMPTY + 8 * x));
-                    // staging [64 queries][128 features] fp32: 4 blocks of 32 features x 64 rows
-                    const uint32_t blk = stage + (uint32_t)quarter * 8192 + ((lane & 3) << 2);
-#pragma unroll
-                    for (int u = 0; u < 32; ++u) {
-                        const uint32_t row = 32 * ch + u;
-                        st_shared_f32(blk + row * 128 + ((((uint32_t)lane >> 2) ^ (row & 7u)) << 4),
-                                      v[u] * p.scale);
-                    }
-                }
-                fence_proxy_async_smem();
-                ok = named_bar_and(1, C::NCOMPUTE, ok);
-                if (ok && threadIdx.x == 0) {
-                    for (int b = 0; b < 4; ++b) tma_reduce_add_3d(&tm_dq64, stage + b * 8192, b * 32, h, q0 + 64 * x);
-                    bulk_commit();
                 }
             }
         }
-        if (threadIdx.x == 0) bulk_wait_all();
         // ------------------------------ dK, dV ---------------------------------
         if (ok) ok = mbar_wait(bar(C::B_DKVFULL), 0, p.status, 52);
         ok = __all_sync(0xffffffffu, ok);

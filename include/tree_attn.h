@@ -78,7 +78,7 @@ typedef struct {
                                  kernels run 128 only; other sizes (1..1024)
                                  are accepted for inspecting the plan.        */
     int32_t bwd_chunk_qtiles; /* max q-tiles per backward work item; 0 = auto:
-                                 max(8, ceil(nonempty tile blocks / 1216))    */
+                                 max(24, ceil(nonempty tile blocks / 600))    */
 } tree_attn_plan_opts_t;
 
 typedef struct {

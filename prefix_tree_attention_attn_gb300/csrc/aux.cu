@@ -22,29 +22,34 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
     return *reinterpret_cast<uint16_t*>(&h);
 }
 
-// One warp per (row i, head h); rows [0, Npad).
+// d/8 lanes per (row i, head h), 8 features (16 bytes of O and of dO) each;
+// rows [0, Npad).
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
-    const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
+    const int lanes = p.d >> 3;                                   // 16 (d = 128) or 8 (d = 64)
+    const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t pair = gid / lanes;
+    const int sub = (int)(gid % lanes);
     const int64_t total = (int64_t)p.Npad * p.hq;
-    if (wid >= total) return;
-    const int i = (int)(wid / p.hq), h = (int)(wid % p.hq);
+    const bool live = pair < total;
+    const int i = live ? (int)(pair / p.hq) : 0, h = live ? (int)(pair % p.hq) : 0;
     float acc = 0.f;
-    if (i < p.N) {
-        const size_t base = ((size_t)i * p.hq + h) * p.d;
-        for (int x = lane * 4; x < p.d; x += 128) {
-            const uint2 ow = *reinterpret_cast<const uint2*>(p.o + base + x);
-            const uint2 dw = *reinterpret_cast<const uint2*>(p.dout + base + x);
-            acc += bf16_bits_to_float(ow.x & 0xffff) * bf16_bits_to_float(dw.x & 0xffff);
-            acc += bf16_bits_to_float(ow.x >> 16) * bf16_bits_to_float(dw.x >> 16);
-            acc += bf16_bits_to_float(ow.y & 0xffff) * bf16_bits_to_float(dw.y & 0xffff);
-            acc += bf16_bits_to_float(ow.y >> 16) * bf16_bits_to_float(dw.y >> 16);
-            *reinterpret_cast<float4*>(p.dq_acc + base + x) = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-    }
+    if (live && i < p.N) {
+        const size_t off = ((size_t)i * p.hq + h) * p.d + sub * 8;
+        const uint4 ow = *reinterpret_cast<const uint4*>(p.o + off);
+        const uint4 dw = *reinterpret_cast<const uint4*>(p.dout + off);
+        const uint32_t ov[4] = {ow.x, ow.y, ow.z, ow.w}, dv[4] = {dw.x, dw.y, dw.z, dw.w};
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) {
+        for (int k = 0; k < 4; ++k) {
+            acc += bf16_bits_to_float(ov[k] & 0xffff) * bf16_bits_to_float(dv[k] & 0xffff);
+            acc += bf16_bits_to_float(ov[k] >> 16) * bf16_bits_to_float(dv[k] >> 16);
+        }
+        float4* z = reinterpret_cast<float4*>(p.dq_acc + off);
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    // sum over the lanes of this (row, head): aligned groups of `lanes` lanes
+    for (int o = lanes >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (live && sub == 0) {
         const size_t k = (size_t)h * p.Npad + i;
         p.delta[k] = acc;
         p.lse2[k] = i < p.N ? p.lse[(size_t)h * p.N + i] * 1.4426950408889634f : INFINITY;
@@ -76,10 +81,26 @@ __global__ void __launch_bounds__(256) dkv_reduce_kernel(const BwdPostParams p) 
     for (int e = threadIdx.x * 4; e < per_tile; e += blockDim.x * 4) {
         const int r = e / p.d, x = e % p.d;
         const int j = c * 128 + r;
+        // ascending chunk order (the same additions on every run); loads are issued
+        // four at a time so that they overlap
+        const size_t stride = (size_t)p.hkv * 2 * per_tile;
+        const float* src = p.part + (((size_t)base * p.hkv + hk) * 2 + which) * per_tile + e;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int k = 0; k < nslot; ++k) {
-            const float4 v = *reinterpret_cast<const float4*>(
-                p.part + (((size_t)(base + k) * p.hkv + hk) * 2 + which) * per_tile + e);
+        int k = 0;
+        for (; k + 4 <= nslot; k += 4) {
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = __ldg(reinterpret_cast<const float4*>(src + (size_t)(k + u) * stride));
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                acc.x += v[u].x;
+                acc.y += v[u].y;
+                acc.z += v[u].z;
+                acc.w += v[u].w;
+            }
+        }
+        for (; k < nslot; ++k) {
+            const float4 v = __ldg(reinterpret_cast<const float4*>(src + (size_t)k * stride));
             acc.x += v.x;
             acc.y += v.y;
             acc.z += v.z;
@@ -97,8 +118,8 @@ __global__ void __launch_bounds__(256) dkv_reduce_kernel(const BwdPostParams p) 
 }  // namespace
 
 cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t stream) {
-    const int64_t warps = (int64_t)p.Npad * p.hq;
-    const int64_t blocks = (warps * 32 + 255) / 256;
+    const int64_t threads = (int64_t)p.Npad * p.hq * (p.d / 8);
+    const int64_t blocks = (threads + 255) / 256;
     if (blocks > INT32_MAX) return cudaErrorInvalidValue;
     bwd_pre_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p);
     return cudaGetLastError();

@@ -221,7 +221,7 @@ int build_plan(const int32_t* parent, const int32_t* seg_len, int32_t n, const t
         // q-tiles share one chunk index; items run chunk by chunk (then longest
         // first), which keeps the dQ rows they accumulate into resident in L2.
         const int64_t entries = (int64_t)P->qt_kv.size();
-        int32_t S = chunk_opt > 0 ? chunk_opt : (int32_t)std::max<int64_t>(8, ceil_div(entries, 1216));
+        int32_t S = chunk_opt > 0 ? chunk_opt : (int32_t)std::max<int64_t>(24, ceil_div(entries, 600));
         P->chunk = S;
         std::vector<int32_t> items;   // {c, t0, t1, slot} plus a sort key below
         std::vector<int32_t> chunk_of;

@@ -214,6 +214,24 @@ def run_reference(args):
 # the GPU arm
 # ---------------------------------------------------------------------------
 
+def max_over_ranks(local_ms: float, world: int, device=None) -> float:
+    """The slowest rank's timed-region length (every rank runs its own tree;
+    the job is done when the last one is)."""
+    if world <= 1:
+        return float(local_ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(local_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job useful TFLOP/s: the units all ranks processed over the
+    slowest rank's time (weak scaling: each rank holds one tree)."""
+    return flops_per_step * steps * world / (max_ms / 1e3) / 1e12
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -301,11 +319,8 @@ def run_ours(args):
     per = [[e[i].elapsed_time(e[i + 1]) for i in range(4)] for e in evs]   # fwd, pre, main, post (ms)
     step_ms = [sum(p) for p in per]
     total_ms = sum(step_ms)
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_max_ms = float(t.item())
-    value = flops_step * args.steps * world / (total_max_ms / 1e3) / 1e12
+    total_max_ms = max_over_ranks(total_ms, world, dev)
+    value = job_throughput(flops_step, args.steps, world, total_max_ms)
     fwd_ms = statistics.mean(p[0] for p in per)
     main_ms = statistics.mean(p[2] for p in per)
     pre_ms = statistics.mean(p[1] for p in per)

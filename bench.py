@@ -327,8 +327,8 @@ def run_ours(args):
     post_ms = statistics.mean(p[3] for p in per)
 
     peak_burst, peak_sus, peak_src = measured_peaks()
-    # the backward's tensor-core kernel is bwd_pp_kernel (bwd_pp.cu) for d = 128, bwd_kernel (bwd.cu) else
-    bwd_name, bwd_src = ("bwd_pp_kernel", "bwd_pp.cu") if d == 128 else ("bwd_kernel", "bwd.cu")
+    # the backward's tensor-core kernel is bwd_fs_kernel (bwd_fs.cu) for d = 128, bwd_kernel (bwd.cu) else
+    bwd_name, bwd_src = ("bwd_fs_kernel", "bwd_fs.cu") if d == 128 else ("bwd_kernel", "bwd.cu")
     dominant = (bwd_name, main_ms, f_bwd, bwd_src) if main_ms >= fwd_ms else ("fwd_kernel", fwd_ms, f_fwd, "fwd.cu")
     achieved = dominant[2] / (dominant[1] / 1e3) / 1e12
     src_hash = kernel_source_hash([dominant[3], "ptx.cuh"])

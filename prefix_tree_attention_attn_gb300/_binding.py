@@ -1,4 +1,4 @@
-"""ctypes declarations of the C ABI in include/tree_attn.h (marshalling only)."""
+"""ctypes declarations of the C ABI in include/*.h (marshalling only)."""
 from __future__ import annotations
 
 import ctypes as C
@@ -8,6 +8,7 @@ from . import build as _build
 
 c_int32_p = C.POINTER(C.c_int32)
 c_uint8_p = C.POINTER(C.c_uint8)
+c_int64_p = C.POINTER(C.c_int64)
 
 
 class PlanOpts(C.Structure):
@@ -30,7 +31,7 @@ class PlanArrays(C.Structure):
                 ("bwd_items", c_int32_p)]
 
 
-# name -> (restype, argtypes); every symbol include/tree_attn.h declares
+# name -> (restype, argtypes); every symbol include/*.h declares
 SIGNATURES = {
     "tree_attn_plan": (C.c_int, [c_int32_p, c_int32_p, C.c_int32, C.POINTER(PlanOpts), C.POINTER(C.c_void_p)]),
     "tree_attn_plan_info": (C.c_int, [C.c_void_p, C.POINTER(PlanInfo)]),
@@ -54,6 +55,13 @@ SIGNATURES = {
     "tree_attn_get_device_status": (C.c_int, [C.c_void_p]),
     "tree_attn_plan_destroy": (None, [C.c_void_p]),
     "tree_attn_strerror": (C.c_char_p, [C.c_int]),
+    # include/tree_batch.h
+    "tree_attn_batch_work": (C.c_int, [C.c_int32, c_int32_p, c_int32_p, c_int32_p, c_int64_p, c_int64_p]),
+    "tree_attn_batch_assign": (C.c_int, [C.c_int32, c_int64_p, C.c_int32, c_int32_p, c_int64_p]),
+    "tree_attn_batch_microbatches": (C.c_int, [C.c_int32, c_int64_p, c_int64_p, c_int32_p, C.c_int32, C.c_int64,
+                                               c_int32_p, c_int32_p]),
+    "tree_attn_batch_forest": (C.c_int, [C.c_int32, c_int32_p, c_int32_p, c_int32_p, c_uint8_p, c_int32_p,
+                                         c_int32_p, c_int32_p, c_int32_p]),
 }
 
 _LIB = None

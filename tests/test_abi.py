@@ -1,5 +1,5 @@
-"""The C-ABI library loads, exports every symbol include/tree_attn.h declares,
-and rejects bad arguments on the host (CPU only; no compute call is made)."""
+"""The C-ABI library loads, exports every symbol include/*.h declares, and
+rejects bad arguments on the host (CPU only; no compute call is made)."""
 import ctypes as C
 import os
 import re
@@ -10,11 +10,12 @@ import pytest
 from prefix_tree_attention_attn_gb300 import _binding as B
 from prefix_tree_attention_attn_gb300 import TreePlan
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "tree_attn.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+HEADER = os.path.join(INCLUDE, "tree_attn.h")
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    text = "".join(open(os.path.join(INCLUDE, f)).read() for f in sorted(os.listdir(INCLUDE)) if f.endswith(".h"))
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(tree_attn_[a-z_]+)\s*\(", text)))
 

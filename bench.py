@@ -52,6 +52,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-expanded", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the CPU sample")
+    ap.add_argument("--extras", action="store_true",
+                    help="instead of the step, time the calls around it (tree batching, loss boundary, "
+                         "subtree advantages); one JSON line each")
     return ap.parse_args()
 
 
@@ -449,8 +452,112 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_extras(args):
+    """The calls around the attention, each timed on its own: host batching of
+    many trees, weights folded into dO, per-trajectory log-probs from compact
+    logits (vocabulary 152,064, the Qwen2.5 LM-head width), subtree advantages."""
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from prefix_tree_attention_attn_gb300 import TreePlan
+    from prefix_tree_attention_attn_gb300 import batch as TB
+    from prefix_tree_attention_attn_gb300 import loss as TL
+    from workloads import tensors as WX
+    from workloads import trees as WT
+
+    hbm = None
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            hbm = float(json.load(f)["hbm_gbs"])
+    except Exception:
+        hbm = 6800.0
+
+    # -- batching: 2048 trees (segment trees and GRPO stars of varied seeds), 8 replicas
+    trees = []
+    for sd in range(1024):
+        a, b = WT.segment_tree(seed=100 + sd), WT.grpo_star_tree(seed=5000 + sd)
+        trees += [(a.parent, a.seg_len), (b.parent, b.seg_len)]
+    t0 = time.perf_counter()
+    reps = 5
+    for _ in range(reps):
+        pairs, toks = TB.batch_work(trees)
+        rep, load = TB.batch_assign(pairs, 8)
+        n_forests = 0
+        for r in range(8):
+            mb, n_mb = TB.batch_microbatches(pairs, toks, rep, r, 65536)
+            for m in range(n_mb):
+                TB.batch_forest(trees, mb == m)
+                n_forests += 1
+    host_ms = (time.perf_counter() - t0) * 1e3 / reps
+    print(json.dumps({"metric": "tree batching (work, LPT over 8 replicas, 64k-token microbatches, forests)",
+                      "value": len(trees) / (host_ms / 1e3), "unit": "trees/s", "ms_per_batch": host_ms,
+                      "config": {"trees": len(trees), "replicas": 8, "microbatches": n_forests,
+                                 "max_replica_pairs_over_mean": float(load.max() / load.mean())},
+                      "dtype": "int64", "cores": 1}))
+
+    dev = torch.device("cuda:0")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def timed(fn, iters=20, warm=3):
+        for _ in range(warm):
+            fn()
+        ms = []
+        for _ in range(iters):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        return statistics.median(ms)
+
+    t = WT.load_tree("grpo_star")
+    heads, rec = WX.HEADS["grpo_star"], WX.VALUE_RECIPES["grpo_star"]
+    plan = TreePlan(t.parent, t.seg_len)
+    x = WX.draw_inputs(t.n_tokens, heads, rec, 1000 + WX.SEEDS["grpo_star"], device="cuda")
+    mult, _ = TL.token_info(plan)
+    w = torch.as_tensor(mult, dtype=torch.float32, device=dev)
+    do = x["do"]
+    out = torch.empty_like(do)
+    ms = timed(lambda: TL.scale_rows(do, w, out=out))
+    nbytes = 2 * do.numel() * 2 + w.numel() * 4
+    print(json.dumps({"metric": "multiplicity weights folded into dO (scale_rows)", "value": nbytes / ms / 1e6,
+                      "unit": "GB/s", "ms": ms, "roofline": {"bound": "hbm", "peak": hbm, "frac": nbytes / ms / 1e6 / hbm},
+                      "config": {"workload": "grpo_star dO [11167, 32, 128] bf16"}, "dtype": "bf16"}))
+
+    V = 152064
+    g = torch.Generator(device="cuda").manual_seed(9)
+    logits = (torch.randn(t.n_tokens, V, generator=g, device=dev) * 2.0).to(torch.bfloat16)
+    tokens = torch.randint(0, V, (t.n_tokens,), generator=g, device=dev, dtype=torch.int32)
+    lse, lp = TL.traj_logprobs(plan, logits, tokens)
+    ms = timed(lambda: TL.traj_logprobs(plan, logits, tokens, row_lse=lse, out=lp), iters=10)
+    nbytes = logits.numel() * 2 + lp.numel() * (4 + 8 + 4 + 2) + t.n_tokens * 4
+    print(json.dumps({"metric": "per-trajectory next-token log-probs from compact logits", "value": nbytes / ms / 1e6,
+                      "unit": "GB/s", "ms": ms, "roofline": {"bound": "hbm", "peak": hbm, "frac": nbytes / ms / 1e6 / hbm},
+                      "config": {"workload": "grpo_star logits [11167, 152064] bf16", "predictions": lp.numel(),
+                                 "expanded_rows_avoided": int(t.n_expanded - t.n_tokens)}, "dtype": "bf16"}))
+    del logits
+
+    ta = WT.load_tree("agentic_tree")
+    pa = TreePlan(ta.parent, ta.seg_len)
+    L, _ = TL.trajectory_info(pa)
+    r = torch.randn(L, device=dev)
+    TL.subtree_advantage(pa, r, flags=TL.NORM_STD)
+    ms = timed(lambda: TL.subtree_advantage(pa, r, flags=TL.NORM_STD), iters=20)
+    print(json.dumps({"metric": "subtree advantages (per trajectory, node and compact token)", "value": ms * 1e3,
+                      "unit": "us", "higher_is_better": False,
+                      "config": {"workload": "agentic_tree", "nodes": ta.n_nodes, "leaves": L,
+                                 "tokens": ta.n_tokens}, "dtype": "f32"}))
+
+
 def main():
     args = parse_args()
+    if args.extras:
+        run_extras(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

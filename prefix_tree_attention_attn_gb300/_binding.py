@@ -62,6 +62,15 @@ SIGNATURES = {
                                                c_int32_p, c_int32_p]),
     "tree_attn_batch_forest": (C.c_int, [C.c_int32, c_int32_p, c_int32_p, c_int32_p, c_uint8_p, c_int32_p,
                                          c_int32_p, c_int32_p, c_int32_p]),
+    # include/tree_loss.h
+    "tree_attn_plan_trajectory_info": (C.c_int, [C.c_void_p, c_int32_p, c_int64_p]),
+    "tree_attn_plan_trajectories": (C.c_int, [C.c_void_p, c_int32_p, c_int64_p, c_int32_p]),
+    "tree_attn_plan_token_info": (C.c_int, [C.c_void_p, c_int32_p, c_int32_p]),
+    "tree_attn_scale_rows": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p]),
+    "tree_attn_traj_logprobs": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p,
+                                          C.c_void_p]),
+    "tree_attn_subtree_advantage": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_float, C.c_void_p,
+                                              C.c_void_p, C.c_void_p, C.c_void_p]),
 }
 
 _LIB = None

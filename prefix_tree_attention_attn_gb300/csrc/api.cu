@@ -85,6 +85,8 @@ int launch_main(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUten
     return e == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
 }
 
+}  // namespace
+
 int current_device(int* dev) {
     if (cudaGetDevice(dev) != cudaSuccess) return TREE_ATTN_ERR_NO_DEVICE;
     if (*dev < 0 || *dev >= kMaxDevices) return TREE_ATTN_ERR_NO_DEVICE;
@@ -94,6 +96,8 @@ int current_device(int* dev) {
     if (major != 10 || minor != 3) return TREE_ATTN_ERR_NO_DEVICE;
     return TREE_ATTN_OK;
 }
+
+namespace {
 
 // Upload (once per device) the tables the kernels read.
 int ensure_device(tree_attn_plan_s* P, DevicePlan** out) {
@@ -548,8 +552,11 @@ void tree_attn_plan_destroy(tree_attn_plan_t P) {
     int cur = -1;
     bool have = cudaGetDevice(&cur) == cudaSuccess;
     for (int dev = 0; dev < kMaxDevices; ++dev) {
-        if (!P->dev[dev].ready) continue;
-        if (cudaSetDevice(dev) == cudaSuccess) cudaFree(P->dev[dev].base);
+        if (!P->dev[dev].ready && !P->dev[dev].traj_ready) continue;
+        if (cudaSetDevice(dev) == cudaSuccess) {
+            if (P->dev[dev].ready) cudaFree(P->dev[dev].base);
+            if (P->dev[dev].traj_ready) cudaFree(P->dev[dev].traj_base);
+        }
     }
     if (have) cudaSetDevice(cur);
     cudaGetLastError();

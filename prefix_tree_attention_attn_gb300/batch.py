@@ -3,11 +3,11 @@ ancestor-pair work, LPT assignment to data-parallel replicas, token-capped
 microbatches, and the packed forest of a group of trees.  Host only; the work
 runs in the C++ library, this module marshals arguments.
 
-    trees = [(parent, seg_len), ...]          # parent indices local to each tree
-    pairs, tokens = batch_work(trees)
+    batch = TreeBatch([(parent, seg_len), ...])   # parent indices local to each tree
+    pairs, tokens = batch.work()
     replica_of, load = batch_assign(pairs, n_replicas)
     mb_of, n_mb = batch_microbatches(pairs, tokens, replica_of, replica=0, max_tokens=65536)
-    parent, seg_len, tree_of = batch_forest(trees, mb_of == 0)   # one plan per microbatch
+    parent, seg_len, tree_of = batch.forest(mb_of == 0)   # one plan per microbatch
 """
 from __future__ import annotations
 
@@ -46,15 +46,39 @@ def _concat(trees: Sequence[Tuple[Sequence[int], Sequence[int]]]):
     return ptr, parent, seg
 
 
+class TreeBatch:
+    """Many trees concatenated once for repeated batching calls."""
+
+    def __init__(self, trees):
+        self.n = len(trees)
+        self.ptr, self.parent, self.seg = _concat(trees)
+
+    def work(self) -> Tuple[np.ndarray, np.ndarray]:
+        """(ancestor pairs, compact tokens) of each tree."""
+        pairs, tokens = np.zeros(self.n, np.int64), np.zeros(self.n, np.int64)
+        B.check(B.load().tree_attn_batch_work(self.n, _p32(self.ptr), _p32(self.parent), _p32(self.seg),
+                                              _p64(pairs), _p64(tokens)), "tree_attn_batch_work")
+        return pairs, tokens
+
+    def forest(self, select) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
+        """The forest of the selected trees: (parent, seg_len, source tree of each node)."""
+        sel = np.ascontiguousarray(np.asarray(select, dtype=bool).astype(np.uint8))
+        if len(sel) != self.n:
+            raise ValueError("select needs one flag per tree")
+        sizes = np.diff(self.ptr)
+        total = int(sizes[sel.astype(bool)].sum()) if self.n else 0
+        op, os_, ot = (np.zeros(max(total, 1), np.int32) for _ in range(3))
+        k = C.c_int32(0)
+        B.check(B.load().tree_attn_batch_forest(self.n, _p32(self.ptr), _p32(self.parent), _p32(self.seg),
+                                                sel.ctypes.data_as(B.c_uint8_p), _p32(op), _p32(os_), _p32(ot),
+                                                C.byref(k)), "tree_attn_batch_forest")
+        m = int(k.value)
+        return op[:m], os_[:m], ot[:m]
+
+
 def batch_work(trees) -> Tuple[np.ndarray, np.ndarray]:
     """(ancestor pairs, compact tokens) of each tree."""
-    lib = B.load()
-    ptr, parent, seg = _concat(trees)
-    n = len(trees)
-    pairs, tokens = np.zeros(n, np.int64), np.zeros(n, np.int64)
-    B.check(lib.tree_attn_batch_work(n, _p32(ptr), _p32(parent), _p32(seg), _p64(pairs), _p64(tokens)),
-            "tree_attn_batch_work")
-    return pairs, tokens
+    return TreeBatch(trees).work()
 
 
 def batch_assign(work, n_replicas: int) -> Tuple[np.ndarray, np.ndarray]:
@@ -81,16 +105,4 @@ def batch_microbatches(work, tokens, replica_of, replica: int, max_tokens: int) 
 
 def batch_forest(trees, select) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
     """The forest of the selected trees: (parent, seg_len, source tree of each node)."""
-    lib = B.load()
-    ptr, parent, seg = _concat(trees)
-    sel = np.ascontiguousarray(np.asarray(select, dtype=bool).astype(np.uint8))
-    if len(sel) != len(trees):
-        raise ValueError("select needs one flag per tree")
-    total = int(sum(len(p) for (p, _), s in zip(trees, sel) if s))
-    op, os_, ot = (np.zeros(max(total, 1), np.int32) for _ in range(3))
-    n = C.c_int32(0)
-    B.check(lib.tree_attn_batch_forest(len(trees), _p32(ptr), _p32(parent), _p32(seg),
-                                       sel.ctypes.data_as(B.c_uint8_p), _p32(op), _p32(os_), _p32(ot), C.byref(n)),
-            "tree_attn_batch_forest")
-    k = int(n.value)
-    return op[:k], os_[:k], ot[:k]
+    return TreeBatch(trees).forest(select)

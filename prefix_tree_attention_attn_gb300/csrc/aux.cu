@@ -23,14 +23,16 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
 }
 
 // d/8 lanes per (row i, head h), 8 features (16 bytes of O and of dO) each;
-// rows [0, Npad).
+// rows [0, Npad), last rows first: the first q-tiles' dQ accumulator rows and
+// dO rows, which the backward's first work items touch, are then the ones
+// written or read most recently and still in L2.
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
     const int lanes = p.d >> 3;                                   // 16 (d = 128) or 8 (d = 64)
     const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t pair = gid / lanes;
-    const int sub = (int)(gid % lanes);
     const int64_t total = (int64_t)p.Npad * p.hq;
-    const bool live = pair < total;
+    const int64_t pair = total - 1 - gid / lanes;
+    const int sub = (int)(gid % lanes);
+    const bool live = pair >= 0;
     const int i = live ? (int)(pair / p.hq) : 0, h = live ? (int)(pair % p.hq) : 0;
     float acc = 0.f;
     if (live && i < p.N) {
@@ -68,17 +70,21 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
     reinterpret_cast<uint2*>(dst)[k] = w;
 }
 
-// One block per (split kv-tile, kv-head, dK|dV); thread = 4 consecutive
-// elements of the 128 x d tile.
+// One block per (split kv-tile, kv-head, dK|dV, group of 16 rows); thread = 4
+// consecutive elements of the group's 16 x d slice of the 128 x d tile.
+constexpr int kDkvRowGroups = 8;
 __global__ void __launch_bounds__(256) dkv_reduce_kernel(const BwdPostParams p) {
-    const int which = blockIdx.x & 1;
-    const int hk = (blockIdx.x >> 1) % p.hkv;
-    const int si = (blockIdx.x >> 1) / p.hkv;
+    const int rg = blockIdx.x % kDkvRowGroups;
+    const int rest = blockIdx.x / kDkvRowGroups;
+    const int which = rest & 1;
+    const int hk = (rest >> 1) % p.hkv;
+    const int si = (rest >> 1) / p.hkv;
     const int4 sp = reinterpret_cast<const int4*>(p.splits)[si];
     const int c = sp.x, base = sp.y, nslot = sp.z;
     const int per_tile = 128 * p.d;
+    const int per_group = per_tile / kDkvRowGroups;
     uint16_t* out = which == 0 ? p.dk : p.dv;
-    for (int e = threadIdx.x * 4; e < per_tile; e += blockDim.x * 4) {
+    for (int e = rg * per_group + threadIdx.x * 4; e < (rg + 1) * per_group; e += blockDim.x * 4) {
         const int r = e / p.d, x = e % p.d;
         const int j = c * 128 + r;
         // ascending chunk order (the same additions on every run); loads are issued
@@ -133,7 +139,7 @@ cudaError_t launch_bwd_post(const BwdPostParams& p, cudaStream_t stream) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (p.n_splits > 0) {
-        dkv_reduce_kernel<<<p.n_splits * p.hkv * 2, 256, 0, stream>>>(p);
+        dkv_reduce_kernel<<<p.n_splits * p.hkv * 2 * kDkvRowGroups, 256, 0, stream>>>(p);
         e = cudaGetLastError();
     }
     return e;

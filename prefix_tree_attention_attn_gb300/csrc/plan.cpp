@@ -222,8 +222,25 @@ int build_plan(const int32_t* parent, const int32_t* seg_len, int32_t n, const t
         // multiples of S, so that the items of every kv-tile that feed the same
         // q-tiles share one chunk index; items run chunk by chunk (then longest
         // first), which keeps the dQ rows they accumulate into resident in L2.
-        const int64_t entries = (int64_t)P->qt_kv.size();
-        int32_t S = chunk_opt > 0 ? chunk_opt : (int32_t)std::max<int64_t>(24, ceil_div(entries, 600));
+        // Auto size: 24 q-tiles, doubled while the split kv-tiles would need more
+        // than max(2048, 8 T) partial dK/dV slots.  Short chunks keep the dQ rows
+        // that concurrently running items add into resident in L2 (a sweep on the
+        // long shared-context tree: 2.07 s of backward at 1,775 q-tiles per chunk,
+        // 1.34 s at 32-64); the slot cap bounds the partials' memory.
+        auto slots_for = [&](int64_t S) {
+            int64_t n = 0;
+            for (int32_t c = 0; c < T; ++c) {
+                const int64_t nc = (P->kv_qhi[c] - 1) / S - P->kv_qlo[c] / S + 1;
+                if (nc > 1) n += nc;
+            }
+            return n;
+        };
+        int64_t S64 = chunk_opt;
+        if (S64 <= 0) {
+            S64 = 24;
+            while (S64 < T && slots_for(S64) > std::max<int64_t>(2048, 8 * (int64_t)T)) S64 *= 2;
+        }
+        const int32_t S = (int32_t)std::min<int64_t>(S64, INT32_MAX);
         P->chunk = S;
         std::vector<int32_t> items;   // {c, t0, t1, slot} plus a sort key below
         std::vector<int32_t> chunk_of;

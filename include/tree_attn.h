@@ -209,6 +209,14 @@ size_t tree_attn_noalloc_scratch_bytes(void);
  * an error return early and leave their outputs incomplete. */
 int tree_attn_get_device_status(void* stream);
 
+/* Self-test of the kernels' failure path: launches one thread that waits on a
+ * barrier nothing completes, bounded by limit_ms (1..2000), so the wait runs
+ * out, records TREE_ATTN_ERR_DEVICE_TIMEOUT - 1000 * 99 in the device status
+ * word and the kernel returns -- the same path every bounded wait of the
+ * attention kernels takes, with no fault and the context still usable.  Read
+ * the result with tree_attn_get_device_status. */
+int tree_attn_selftest_wait_timeout(int32_t limit_ms, void* stream);
+
 /* Free the plan and its device copies (call after work using it finished). */
 void tree_attn_plan_destroy(tree_attn_plan_t plan);
 

@@ -53,6 +53,7 @@ SIGNATURES = {
                                         C.c_int32, C.c_float, C.c_void_p]),
     "tree_attn_noalloc_scratch_bytes": (C.c_size_t, []),
     "tree_attn_get_device_status": (C.c_int, [C.c_void_p]),
+    "tree_attn_selftest_wait_timeout": (C.c_int, [C.c_int32, C.c_void_p]),
     "tree_attn_plan_destroy": (None, [C.c_void_p]),
     "tree_attn_strerror": (C.c_char_p, [C.c_int]),
     # include/tree_batch.h

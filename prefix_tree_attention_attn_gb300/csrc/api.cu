@@ -539,6 +539,17 @@ int tree_attn_bwd_noalloc(tree_attn_plan_t P, const void* q, const void* k, cons
 
 size_t tree_attn_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
 
+int tree_attn_selftest_wait_timeout(int32_t limit_ms, void* stream) {
+    if (limit_ms < 1 || limit_ms > 2000) return TREE_ATTN_ERR_INVALID_ARG;
+    int dev;
+    int st = current_device(&dev);
+    if (st) return st;
+    int* status = nullptr;
+    if ((st = status_ptr(dev, &status))) return st;
+    treeattn::launch_wait_selftest(status, (uint64_t)limit_ms * 1000000ull, static_cast<cudaStream_t>(stream));
+    return cudaGetLastError() == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
+}
+
 int tree_attn_get_device_status(void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return TREE_ATTN_ERR_CUDA;
     int v = 0, zero = 0;

@@ -121,7 +121,26 @@ __global__ void __launch_bounds__(256) dkv_reduce_kernel(const BwdPostParams p) 
     }
 }
 
+// One thread waits, with the given limit, on a barrier that no one completes:
+// the timeout path of every bounded wait in the kernels, run on purpose.  The
+// wait ends by itself and the kernel returns; nothing faults.
+__global__ void wait_selftest_kernel(int* status, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar_mem;
+    const uint32_t bar = smem_u32(&bar_mem);
+    mbar_init(bar, 1);
+    fence_mbar_init();
+    if (mbar_try_wait(bar, 0)) return;
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 <= limit_ns)
+        if (mbar_try_wait(bar, 0)) return;
+    report_status(status, -10 - 1000 * 99);
+}
+
 }  // namespace
+
+void launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t stream) {
+    wait_selftest_kernel<<<1, 1, 0, stream>>>(status, limit_ns);
+}
 
 cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t stream) {
     const int64_t threads = (int64_t)p.Npad * p.hq * (p.d / 8);

@@ -68,5 +68,7 @@ cudaError_t launch_bwd_pp(const CUtensorMap* tq, const CUtensorMap* tk, const CU
 cudaError_t launch_bwd_fs(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv, const CUtensorMap* tdo,
                           const CUtensorMap* tdq, const BwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_bwd_post(const BwdPostParams& p, cudaStream_t stream);
+// a bounded wait that runs out on purpose (site 99)
+void launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t stream);
 
 }  // namespace treeattn

@@ -95,3 +95,21 @@ def test_sibling_order_does_not_matter(lib, cuda_device):
     for x, y, tol in ((b[0], o[ii], 1e-2), (b[2], dq[ii], 1e-2), (b[3], dk[ii], 1e-2), (b[4], dv[ii], 1e-2)):
         assert close(x, y, tol)
     assert float((b[1] - lse[:, ii]).abs().max()) <= 1e-2
+
+
+def test_bounded_wait_timeout_is_reported_and_context_survives(lib, cuda_device):
+    """A wait that nothing completes runs out after its limit, the kernel
+    returns and records the timeout; the next calls work normally."""
+    import prefix_tree_attention_attn_gb300._binding as B
+    assert device_status() == 0
+    st = B.load().tree_attn_selftest_wait_timeout(50, None)
+    assert st == 0
+    code = device_status()
+    assert code == -10 - 1000 * 99, code
+    assert B.load().tree_attn_strerror(code).decode().startswith("a bounded device wait")
+    assert device_status() == 0          # read and cleared
+    from .gpu_util import full_parity
+    t = WT.Tree("after", [-1, 0], [130, 70])
+    x = WX.draw_inputs(t.n_tokens, HEADS, WX.ValueRecipe(1, 1, 1, 1, 1), 4)
+    full_parity(t, x["q"], x["k"], x["v"], x["do"], SCALE, tag="after-timeout")
+    assert device_status() == 0

@@ -1,0 +1,71 @@
+"""Linear attention over a rollout tree, the slow and obvious way (test
+infrastructure).
+
+HARTS (abstract): hybrid models mix softmax attention with linear attention,
+whose recurrent state must be carried from a shared prefix into every branch.
+This build's reading (the pages give no formula): per q-head h with kv-head
+g = h // G and a per-kv-head decay gamma_g in (0, 1],
+
+    o_i = scale * sum_{j on i's root-to-node path, j <= i} gamma^(pos_i - pos_j) (q_i . k_j) v_j
+
+with pos the position along the trajectory (gamma = 1: plain causal linear
+attention; gamma < 1: a retention-style decay).  Equivalently, the state
+after token j of a trajectory, S_j = gamma S_(j-1) + k_j v_j^T, gives
+o_i = scale * q_i^T S_i; at a branch point every child starts from its
+parent's final state.
+
+Two formulas, both fp64, on the expanded trajectories (one per leaf, first
+copy of each compact token kept; the copies agree):
+* ``forward_parallel`` -- the double sum above, as masked matrices;
+* ``forward_recurrent`` -- the state recursion token by token.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import layout
+
+
+def _as64(x):
+    return np.asarray(x.float().numpy() if hasattr(x, "float") else x, dtype=np.float64)
+
+
+def forward_parallel(parent, seg_len, q, k, v, decay, scale):
+    """O [N, hq, d] (fp64).  q [N, hq, d], k / v [N, hkv, d], decay [hkv]."""
+    q, k, v = _as64(q), _as64(k), _as64(v)
+    gam = np.asarray(decay, dtype=np.float64)
+    N, hq, d = q.shape
+    hkv = k.shape[1]
+    G = hq // hkv
+    out = np.full((N, hq, d), np.nan)
+    for _, idx in layout.trajectories(parent, seg_len):
+        L = len(idx)
+        pos = np.arange(L)
+        diff = pos[:, None] - pos[None, :]
+        for h in range(hq):
+            g = h // G
+            w = np.where(diff >= 0, gam[g] ** np.maximum(diff, 0), 0.0)
+            s = q[idx, h] @ k[idx, g].T
+            o = scale * (s * w) @ v[idx, g]
+            first = np.isnan(out[idx, h, 0])
+            out[idx[first], h] = o[first]
+    return out
+
+
+def forward_recurrent(parent, seg_len, q, k, v, decay, scale):
+    """The same output from the state recursion, one token at a time."""
+    q, k, v = _as64(q), _as64(k), _as64(v)
+    gam = np.asarray(decay, dtype=np.float64)
+    N, hq, d = q.shape
+    hkv = k.shape[1]
+    G = hq // hkv
+    out = np.full((N, hq, d), np.nan)
+    for _, idx in layout.trajectories(parent, seg_len):
+        for g in range(hkv):
+            S = np.zeros((d, d))
+            for t in idx:
+                S = gam[g] * S + np.outer(k[t, g], v[t, g])
+                for h in range(g * G, (g + 1) * G):
+                    if np.isnan(out[t, h, 0]):
+                        out[t, h] = scale * (q[t, h] @ S)
+    return out

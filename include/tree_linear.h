@@ -1,0 +1,58 @@
+/*
+ * tree_linear.h -- linear attention over a packed rollout tree, chunk by
+ * chunk, with the recurrent state handed from each node to its children
+ * (libtreeattn).
+ *
+ * Section: HARTS abstract -- hybrid models interleave softmax attention with
+ * linear attention; on a rollout tree the linear layers' recurrent state has to
+ * be carried from a shared prefix into every branch.  The pages give no
+ * formula; this library computes, per q-head h (kv-head g = h / (hq / hkv)) and
+ * a decay gamma_g in (0, 1] per kv-head,
+ *
+ *   O_i = scale * sum_{j on i's root-to-node path, j <= i} gamma_g^(pos_i - pos_j) (q_i . k_j) v_j
+ *
+ * (pos = position along the trajectory; gamma = 1 is plain causal linear
+ * attention).  Equivalently S_j = gamma S_{j-1} + k_j v_j^T along each
+ * trajectory and O_i = scale q_i^T S_i; a child's first token continues from
+ * its parent's last state.
+ *
+ * Chunked form: every node's segment is cut into chunks of at most 128
+ * tokens.  Per chunk and kv-head the state increment
+ *   dS_c = sum_{m < L} gamma^(L-1-m) k_m v_m^T               (tensor cores)
+ * then, in packed (depth-first) order, the state entering each chunk
+ *   S_in(first chunk of u) = S_out(parent(u)),  S_in(next) = gamma^L S_in + dS_c
+ * (an elementwise scan, parallel over the d x d state entries), then per chunk
+ * and q-head
+ *   O = scale (diag(gamma^(m+1)) Q S_in + ((Q K^T) o D) V),  D[m, m'] = gamma^(m-m') for m' <= m
+ * (three tensor-core products, the decay mask in registers).
+ *
+ * Tensors as in tree_attn.h: Q, O [N, hq, d] bf16, K, V [N, hkv, d] bf16 in
+ * packed order; decay fp32 [hkv] (device).  d = 128.  The workspace holds the
+ * per-chunk increments and entering states and the per-node exit states
+ * (fp32); contents on entry ignored.  Asynchronous on `stream`.
+ */
+#ifndef TREE_LINEAR_H
+#define TREE_LINEAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "tree_attn.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Chunks of the plan (<= 128 tokens, inside one node each) and the workspace
+ * bytes tree_attn_linear_fwd needs for hkv kv-heads of head_dim d. */
+int tree_attn_linear_workspace_size(tree_attn_plan_t plan, int32_t hkv, int32_t d, int64_t* n_chunks,
+                                    size_t* ws_bytes);
+
+int tree_attn_linear_fwd(tree_attn_plan_t plan, const void* q, const void* k, const void* v, void* o,
+                         const float* decay, int32_t hq, int32_t hkv, int32_t d, float scale,
+                         void* workspace, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TREE_LINEAR_H */

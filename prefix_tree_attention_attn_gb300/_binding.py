@@ -63,6 +63,12 @@ SIGNATURES = {
                                                c_int32_p, c_int32_p]),
     "tree_attn_batch_forest": (C.c_int, [C.c_int32, c_int32_p, c_int32_p, c_int32_p, c_uint8_p, c_int32_p,
                                          c_int32_p, c_int32_p, c_int32_p]),
+    # include/tree_linear.h
+    "tree_attn_linear_workspace_size": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32, c_int64_p,
+                                                  C.POINTER(C.c_size_t)]),
+    "tree_attn_linear_fwd": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                       C.c_int32, C.c_int32, C.c_int32, C.c_float, C.c_void_p, C.c_size_t,
+                                       C.c_void_p]),
     # include/tree_loss.h
     "tree_attn_plan_trajectory_info": (C.c_int, [C.c_void_p, c_int32_p, c_int64_p]),
     "tree_attn_plan_trajectories": (C.c_int, [C.c_void_p, c_int32_p, c_int64_p, c_int32_p]),

@@ -87,6 +87,10 @@ int launch_main(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUten
 
 }  // namespace
 
+int make_tensor_map(CUtensorMap* m, const void* base, int64_t rows, int heads, int d) {
+    return make_tmap(m, base, rows, heads, d);
+}
+
 int current_device(int* dev) {
     if (cudaGetDevice(dev) != cudaSuccess) return TREE_ATTN_ERR_NO_DEVICE;
     if (*dev < 0 || *dev >= kMaxDevices) return TREE_ATTN_ERR_NO_DEVICE;
@@ -199,6 +203,9 @@ WsLayout bwd_layout(const tree_attn_plan_s* P, int hq, int hkv, int d) {
 }
 
 }  // namespace
+
+int get_status_ptr(int dev, int** out) { return status_ptr(dev, out); }
+
 }  // namespace treeattn
 
 using namespace treeattn;
@@ -563,10 +570,11 @@ void tree_attn_plan_destroy(tree_attn_plan_t P) {
     int cur = -1;
     bool have = cudaGetDevice(&cur) == cudaSuccess;
     for (int dev = 0; dev < kMaxDevices; ++dev) {
-        if (!P->dev[dev].ready && !P->dev[dev].traj_ready) continue;
+        if (!P->dev[dev].ready && !P->dev[dev].traj_ready && !P->dev[dev].lin_ready) continue;
         if (cudaSetDevice(dev) == cudaSuccess) {
             if (P->dev[dev].ready) cudaFree(P->dev[dev].base);
             if (P->dev[dev].traj_ready) cudaFree(P->dev[dev].traj_base);
+            if (P->dev[dev].lin_ready) cudaFree(P->dev[dev].lin_base);
         }
     }
     if (have) cudaSetDevice(cur);

@@ -1,0 +1,467 @@
+// Linear attention over a packed rollout tree, chunk by chunk, with the
+// recurrent state handed from every node to its children
+// (include/tree_linear.h).
+//
+// Three kernels per call:
+//   lin_delta_kernel  per (chunk, kv-head): dS = K^T diag(gamma^(L-1-m)) V on
+//                     the tensor core (M = 128 key features, N = 128 value
+//                     features, K = the chunk's tokens), read out of TMEM to
+//                     an fp32 workspace;
+//   lin_scan_kernel   per state entry (d x d x hkv threads): walks the nodes in
+//                     packed order, the entering state of each chunk
+//                     S_in = gamma^L S_in(prev) + dS(prev), a child starting
+//                     from its parent's exit state -- the branch-point handoff;
+//   lin_out_kernel    per (chunk, q-head): S = Q K^T, O = Q S_in (bf16 copy of
+//                     the state as the B operand), then P = S o decay mask
+//                     (registers, written back over S as packed bf16), O rows
+//                     scaled by gamma^(m+1), O += P V; O out as bf16.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+#include <vector>
+
+#include "kernels.h"
+#include "plan.h"
+#include "ptx.cuh"
+#include "tree_linear.h"
+
+namespace treeattn {
+
+namespace {
+
+constexpr int kChunk = 128;
+constexpr int kD = 128;
+constexpr int kTile = kChunk * kD * 2;   // 32 KB bf16 tile
+
+// ---- dS per (chunk, kv-head) -------------------------------------------------
+// warps 0-3: lane r = token row r (scaling V) and key feature r (read-out);
+// warp 4: TMEM owner, lane 0 issues the loads and the MMA.
+constexpr int kDeltaSmem = 1024 + 2 * kTile;
+
+__global__ void __launch_bounds__(160, 1)
+    lin_delta_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                     const int32_t* __restrict__ chunks, const float* __restrict__ decay, int hkv,
+                     float* __restrict__ ds, int* status) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const uint32_t sb = smem_u32(smem);
+    const int warp = threadIdx.x >> 5;
+    if (sb & 1023u) {
+        if (threadIdx.x == 0) report_status(status, -5);
+        return;
+    }
+    const int chunk = blockIdx.x / hkv, g = blockIdx.x % hkv;
+    const int off = chunks[4 * chunk], L = chunks[4 * chunk + 1];
+    const uint32_t b_full = sb, b_done = sb + 8, holder = sb + 16;
+    const uint32_t ka = sb + 1024, va = ka + kTile;
+    if (threadIdx.x == 0) {
+        mbar_init(b_full, 1);
+        mbar_init(b_done, 1);
+        fence_mbar_init();
+    }
+    if (warp == 4) tmem_alloc(holder, 128);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + 16);
+    if (threadIdx.x == 128) {
+        mbar_expect_tx(b_full, 2 * kTile);
+        for (int blk = 0; blk < 2; ++blk) {
+            tma_load_3d(ka + blk * 16384, &tm_k, blk * 64, g, off, b_full);
+            tma_load_3d(va + blk * 16384, &tm_v, blk * 64, g, off, b_full);
+        }
+    }
+    bool ok = mbar_wait(b_full, 0, status, 81);
+    if (warp < 4 && ok) {
+        // V row r times gamma^(L-1-r) (0 past the chunk): the row's 128 bytes in
+        // each 64-feature block stay inside that row under the 128-byte swizzle
+        const int r = threadIdx.x;
+        const float lg = log2f(decay[g]);
+        const float w = r < L ? exp2f((float)(L - 1 - r) * lg) : 0.f;
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+            uint4* row = reinterpret_cast<uint4*>(smem + 1024 + kTile + blk * 16384 + r * 128);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                uint4 x = row[c];
+                uint32_t* u = reinterpret_cast<uint32_t*>(&x);
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    u[e] = pack_bf16x2(__uint_as_float(u[e] << 16) * w, __uint_as_float(u[e] & 0xffff0000u) * w);
+                row[c] = x;
+            }
+        }
+        fence_proxy_async_smem();
+    }
+    ok = __syncthreads_and(ok);
+    if (ok && threadIdx.x == 128) {
+        tc_fence_after();
+        constexpr uint32_t ID = idesc_bf16(128, 128, true, true);   // K^T (MN-major) x V_w (MN-major)
+#pragma unroll
+        for (int k = 0; k < kChunk / 16; ++k)
+            mma_bf16_ss(tmem, sdesc_sw128(ka + k * 2048, 16384, 1024), sdesc_sw128(va + k * 2048, 16384, 1024), ID,
+                        k > 0);
+        mma_commit(b_done);
+    }
+    if (warp < 4) {
+        if (ok) ok = mbar_wait(b_done, 0, status, 82);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+            tc_fence_after();
+            const int r = threadIdx.x;   // key feature
+            const uint32_t lane_base = tmem + ((uint32_t)(warp << 5) << 16);
+            float4* dst = reinterpret_cast<float4*>(ds + (((size_t)chunk * hkv + g) * kD + r) * kD);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                float v[32];
+                tmem_ld32(lane_base + cc * 32, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    dst[cc * 8 + u] = make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 4) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 128);
+    }
+}
+
+// ---- entering states, node by node in packed order ----------------------------
+__global__ void __launch_bounds__(256) lin_scan_kernel(const int32_t* __restrict__ lnodes, int n_nodes,
+                                                     const int32_t* __restrict__ chunks,
+                                                     const float* __restrict__ decay, int hkv,
+                                                     const float* __restrict__ ds, float* __restrict__ s_in,
+                                                     float* __restrict__ s_out) {
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;   // state entry (row * d + col)
+    const int g = blockIdx.y;
+    const size_t dd = (size_t)kD * kD;
+    const float lg = log2f(decay[g]);
+    for (int k = 0; k < n_nodes; ++k) {
+        const int par = lnodes[4 * k], c0 = lnodes[4 * k + 1], nc = lnodes[4 * k + 2];
+        float S = par < 0 ? 0.f : s_out[((size_t)par * hkv + g) * dd + e];
+        for (int c = c0; c < c0 + nc; ++c) {
+            const size_t at = ((size_t)c * hkv + g) * dd + e;
+            s_in[at] = S;
+            S = exp2f((float)chunks[4 * c + 1] * lg) * S + ds[at];
+        }
+        s_out[((size_t)k * hkv + g) * dd + e] = S;
+    }
+}
+
+// ---- outputs per (chunk, q-head) ------------------------------------------------
+// warps 0-3: lane m = query row m of the chunk (and key feature m when staging
+// S_in); warp 4: loads; warp 5: TMEM owner, lane 0 issues the MMAs.
+// TMEM: S / P at columns [0, 128), O at [128, 256).
+constexpr int kOutSmem = 1024 + 4 * kTile;   // Q, K, V, S_in (bf16)
+
+__global__ void __launch_bounds__(192, 1)
+    lin_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const int32_t* __restrict__ chunks,
+                   const float* __restrict__ decay, const float* __restrict__ s_in, uint16_t* __restrict__ out,
+                   int hq, int hkv, float scale, int* status) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const uint32_t sb = smem_u32(smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (sb & 1023u) {
+        if (threadIdx.x == 0) report_status(status, -5);
+        return;
+    }
+    const int chunk = blockIdx.x / hq, h = blockIdx.x % hq, g = h / (hq / hkv);
+    const int off = chunks[4 * chunk], L = chunks[4 * chunk + 1];
+    const uint32_t b_full = sb, b_sin = sb + 8, b_s = sb + 16, b_o1 = sb + 24, b_p = sb + 32, b_o2 = sb + 40;
+    const uint32_t holder = sb + 48;
+    const uint32_t qa = sb + 1024, ka = qa + kTile, va = ka + kTile, sina = va + kTile;
+    if (threadIdx.x == 0) {
+        mbar_init(b_full, 1);
+        mbar_init(b_sin, 128);
+        mbar_init(b_s, 1);
+        mbar_init(b_o1, 1);
+        mbar_init(b_p, 128);
+        mbar_init(b_o2, 1);
+        fence_mbar_init();
+    }
+    if (warp == 5) tmem_alloc(holder, 256);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + 48);
+
+    if (warp == 4) {
+        if (lane == 0) {
+            mbar_expect_tx(b_full, 3 * kTile);
+            for (int blk = 0; blk < 2; ++blk) {
+                tma_load_3d(qa + blk * 16384, &tm_q, blk * 64, h, off, b_full);
+                tma_load_3d(ka + blk * 16384, &tm_k, blk * 64, g, off, b_full);
+                tma_load_3d(va + blk * 16384, &tm_v, blk * 64, g, off, b_full);
+            }
+        }
+    } else if (warp == 5) {
+        if (lane == 0) {
+            constexpr uint32_t ID_S = idesc_bf16(128, 128, false, false);   // Q K^T
+            constexpr uint32_t ID_O = idesc_bf16(128, 128, false, true);    // Q S_in, P V
+            bool ok = mbar_wait(b_full, 0, status, 83);
+            if (ok) {
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < kD / 16; ++k) {
+                    const uint32_t o = (k >> 2) * 16384 + (k & 3) * 32;
+                    mma_bf16_ss(tmem, sdesc_sw128(qa + o, 16, 1024), sdesc_sw128(ka + o, 16, 1024), ID_S, k > 0);
+                }
+                mma_commit(b_s);
+                ok = mbar_wait(b_sin, 0, status, 84);
+            }
+            if (ok) {
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < kD / 16; ++k) {
+                    const uint32_t o = (k >> 2) * 16384 + (k & 3) * 32;
+                    mma_bf16_ss(tmem + 128, sdesc_sw128(qa + o, 16, 1024), sdesc_sw128(sina + k * 2048, 16384, 1024),
+                                ID_O, k > 0);
+                }
+                mma_commit(b_o1);
+                ok = mbar_wait(b_p, 0, status, 85);
+            }
+            if (ok) {
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < kChunk / 16; ++k)
+                    mma_bf16_ts(tmem + 128, tmem + k * 8, sdesc_sw128(va + k * 2048, 16384, 1024), ID_O, 1u);
+                mma_commit(b_o2);
+            }
+        }
+        __syncwarp();
+    } else {
+        const int m = threadIdx.x;   // query row; key feature when staging the state
+        const uint32_t lane_base = tmem + ((uint32_t)(warp << 5) << 16);
+        const float lg = log2f(decay[g]);
+        // S_in (fp32, [key feature][value feature]) -> bf16 B operand, laid out
+        // like a value tile: row = key feature, two 64-column 128B-swizzled blocks
+        {
+            const float4* src = reinterpret_cast<const float4*>(s_in + (((size_t)chunk * hkv + g) * kD + m) * kD);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {   // 8 features per 16-byte chunk
+                const float4 a = src[2 * j], b = src[2 * j + 1];
+                const int blk = j >> 3, cj = j & 7;
+                st_shared_v4(sina + blk * 16384 + sw128_offset(m, cj), pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w),
+                             pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(b_sin);
+        }
+        bool ok = mbar_wait(b_s, 0, status, 86);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+            tc_fence_after();
+            // P[m, m'] = scale * S[m, m'] * gamma^(m - m') for m' <= m and m' < L
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                float v[32];
+                tmem_ld32(lane_base + cc * 32, v);
+                tmem_wait_ld();
+                uint32_t pw[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const int c0 = cc * 32 + 2 * u, c1 = c0 + 1;
+                    const float p0 = (c0 <= m && c0 < L) ? scale * v[2 * u] * exp2f((float)(m - c0) * lg) : 0.f;
+                    const float p1 = (c1 <= m && c1 < L) ? scale * v[2 * u + 1] * exp2f((float)(m - c1) * lg) : 0.f;
+                    pw[u] = pack_bf16x2(p0, p1);
+                }
+                tmem_st16(lane_base + cc * 16, pw);
+            }
+            tmem_wait_st();
+            ok = mbar_wait(b_o1, 0, status, 87);
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+            tc_fence_after();
+            // the carried-in part: scale * gamma^(m+1) * (q_m . S_in)
+            const float f = scale * exp2f((float)(m + 1) * lg);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                float v[32];
+                tmem_ld32(lane_base + 128 + cc * 32, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int u = 0; u < 32; ++u) v[u] *= f;
+                tmem_st32(lane_base + 128 + cc * 32, v);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(b_p);
+            ok = mbar_wait(b_o2, 0, status, 88);
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+            tc_fence_after();
+            uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)(off + m) * hq + h) * kD);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                float v[32];
+                tmem_ld32(lane_base + 128 + cc * 32, v);
+                tmem_wait_ld();
+                if (m < L) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        uint4 w;
+                        w.x = pack_bf16x2(v[8 * u], v[8 * u + 1]);
+                        w.y = pack_bf16x2(v[8 * u + 2], v[8 * u + 3]);
+                        w.z = pack_bf16x2(v[8 * u + 4], v[8 * u + 5]);
+                        w.w = pack_bf16x2(v[8 * u + 6], v[8 * u + 7]);
+                        dst[cc * 4 + u] = w;
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
+int build_lin(tree_attn_plan_s* P) {
+    LinInfo& X = P->lin;
+    if (X.ready) return TREE_ATTN_OK;
+    try {
+        const int32_t n = P->n_nodes;
+        std::vector<int32_t> pos_of(n);
+        for (int32_t k = 0; k < n; ++k) pos_of[P->node_order[k]] = k;
+        X.chunks.clear();
+        X.lnodes.assign(4 * (size_t)n, 0);
+        int32_t nc = 0;
+        for (int32_t k = 0; k < n; ++k) {
+            const int32_t u = P->node_order[k], p = P->parent[u];
+            const int32_t first = nc;
+            for (int32_t o = 0; o < P->seg_len[u]; o += kChunk) {
+                X.chunks.insert(X.chunks.end(), {P->node_off[u] + o, std::min(kChunk, P->seg_len[u] - o), k, 0});
+                ++nc;
+            }
+            X.lnodes[4 * (size_t)k] = p < 0 ? -1 : pos_of[p];
+            X.lnodes[4 * (size_t)k + 1] = first;
+            X.lnodes[4 * (size_t)k + 2] = nc - first;
+        }
+        X.ready = true;
+    } catch (const std::bad_alloc&) {
+        return TREE_ATTN_ERR_OUT_OF_MEMORY;
+    }
+    return TREE_ATTN_OK;
+}
+
+int ensure_lin_device(tree_attn_plan_s* P, DevicePlan** out) {
+    int dev;
+    int st = current_device(&dev);
+    if (st) return st;
+    std::lock_guard<std::mutex> lk(P->mu);
+    if ((st = build_lin(P))) return st;
+    DevicePlan& D = P->dev[dev];
+    if (!D.lin_ready) {
+        const size_t a = (P->lin.chunks.size() + 63) / 64 * 64, b = P->lin.lnodes.size();
+        std::vector<int32_t> h(a + b, 0);
+        std::copy(P->lin.chunks.begin(), P->lin.chunks.end(), h.begin());
+        std::copy(P->lin.lnodes.begin(), P->lin.lnodes.end(), h.begin() + a);
+        void* buf = nullptr;
+        if (cudaMalloc(&buf, h.size() * sizeof(int32_t)) != cudaSuccess) {
+            cudaGetLastError();
+            return TREE_ATTN_ERR_OUT_OF_MEMORY;
+        }
+        if (cudaMemcpy(buf, h.data(), h.size() * sizeof(int32_t), cudaMemcpyHostToDevice) != cudaSuccess) {
+            cudaFree(buf);
+            return TREE_ATTN_ERR_CUDA;
+        }
+        D.lin_base = buf;
+        D.chunks = static_cast<int32_t*>(buf);
+        D.lnodes = static_cast<int32_t*>(buf) + a;
+        D.lin_ready = true;
+    }
+    *out = &D;
+    return TREE_ATTN_OK;
+}
+
+struct LinWs {
+    size_t ds, s_in, s_out, total;
+};
+
+LinWs lin_layout(const tree_attn_plan_s* P, int32_t hkv) {
+    const size_t per = (size_t)hkv * kD * kD * sizeof(float);
+    const size_t nc = P->lin.chunks.size() / 4;
+    LinWs w;
+    w.ds = 0;
+    w.s_in = nc * per;
+    w.s_out = 2 * nc * per;
+    w.total = (2 * nc + (size_t)P->n_nodes) * per;
+    return w;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace
+
+}  // namespace treeattn
+
+using namespace treeattn;
+
+extern "C" {
+
+int tree_attn_linear_workspace_size(tree_attn_plan_t P, int32_t hkv, int32_t d, int64_t* n_chunks, size_t* ws_bytes) {
+    if (!P || hkv <= 0) return TREE_ATTN_ERR_INVALID_ARG;
+    if (d != kD) return TREE_ATTN_ERR_UNSUPPORTED;
+    {
+        std::lock_guard<std::mutex> lk(P->mu);
+        int st = build_lin(P);
+        if (st) return st;
+    }
+    if (n_chunks) *n_chunks = (int64_t)(P->lin.chunks.size() / 4);
+    if (ws_bytes) *ws_bytes = lin_layout(P, hkv).total;
+    return TREE_ATTN_OK;
+}
+
+int tree_attn_linear_fwd(tree_attn_plan_t P, const void* q, const void* k, const void* v, void* o,
+                         const float* decay, int32_t hq, int32_t hkv, int32_t d, float scale, void* workspace,
+                         size_t ws_bytes, void* stream) {
+    if (!P || !q || !k || !v || !o || !decay || hq <= 0 || hkv <= 0 || hq % hkv != 0) return TREE_ATTN_ERR_INVALID_ARG;
+    if (d != kD || P->block != kChunk) return TREE_ATTN_ERR_UNSUPPORTED;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return TREE_ATTN_ERR_INVALID_ARG;
+    for (const void* p : {q, k, v, (const void*)o})
+        if (!aligned(p, 16)) return TREE_ATTN_ERR_ALIGNMENT;
+    if (!aligned(decay, 4) || !aligned(workspace, 256)) return TREE_ATTN_ERR_ALIGNMENT;
+    DevicePlan* D = nullptr;
+    int st = ensure_lin_device(P, &D);
+    if (st) return st;
+    const LinWs w = lin_layout(P, hkv);
+    if (!workspace || ws_bytes < w.total) return TREE_ATTN_ERR_WORKSPACE;
+    const int64_t nc = (int64_t)(P->lin.chunks.size() / 4);
+    if (nc * hq > INT32_MAX || nc * hkv > INT32_MAX) return TREE_ATTN_ERR_TOO_LARGE;
+    CUtensorMap tq, tk, tv;
+    if ((st = make_tensor_map(&tq, q, P->N, hq, d)) || (st = make_tensor_map(&tk, k, P->N, hkv, d)) ||
+        (st = make_tensor_map(&tv, v, P->N, hkv, d)))
+        return st;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int* status = nullptr;
+    if ((st = get_status_ptr(dev, &status))) return st;
+    char* ws = static_cast<char*>(workspace);
+    float* ds = reinterpret_cast<float*>(ws + w.ds);
+    float* s_in = reinterpret_cast<float*>(ws + w.s_in);
+    float* s_out = reinterpret_cast<float*>(ws + w.s_out);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaFuncSetAttribute(lin_delta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDeltaSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(lin_out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kOutSmem) != cudaSuccess)
+        return TREE_ATTN_ERR_CUDA;
+    lin_delta_kernel<<<(unsigned)(nc * hkv), 160, kDeltaSmem, s>>>(tk, tv, D->chunks, decay, hkv, ds, status);
+    if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
+    lin_scan_kernel<<<dim3(kD * kD / 256, hkv), 256, 0, s>>>(D->lnodes, P->n_nodes, D->chunks, decay, hkv, ds, s_in,
+                                                             s_out);
+    if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
+    lin_out_kernel<<<(unsigned)(nc * hq), 192, kOutSmem, s>>>(tq, tk, tv, D->chunks, decay, s_in,
+                                                              static_cast<uint16_t*>(o), hq, hkv, scale, status);
+    return cudaGetLastError() == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -6,6 +6,8 @@
 #include <mutex>
 #include <vector>
 
+#include <cuda.h>
+
 #include "tree_attn.h"
 
 namespace treeattn {
@@ -30,6 +32,18 @@ struct DevicePlan {
                                    //             first token, tokens, node id
     int32_t* leaf_of = nullptr;    // [2*n_leaves] per leaf in packed order: packed node index, id-order index
     bool traj_ready = false;
+    // chunk tables of the linear-attention calls (uploaded on their first use)
+    void* lin_base = nullptr;
+    int32_t* chunks = nullptr;     // [4*n_chunks] {first token, tokens, packed node, 0}
+    int32_t* lnodes = nullptr;     // [4*n_nodes] per packed node {parent's packed index, first chunk, chunks, 0}
+    bool lin_ready = false;
+};
+
+// Chunks of at most 128 tokens inside each node's segment, in packed order.
+struct LinInfo {
+    std::vector<int32_t> chunks;   // as DevicePlan::chunks
+    std::vector<int32_t> lnodes;   // as DevicePlan::lnodes
+    bool ready = false;
 };
 
 // Per-trajectory view of a plan (built on first use): leaves in ascending node
@@ -65,6 +79,7 @@ struct Plan {
     int64_t n_slots = 0;
     std::vector<int32_t> parent, seg_len;   // the tree as given
     TrajInfo traj;                          // guarded by mu
+    LinInfo lin;                            // guarded by mu
 
     std::mutex mu;
     DevicePlan dev[kMaxDevices];
@@ -82,4 +97,9 @@ int build_plan(const int32_t* parent, const int32_t* seg_len, int32_t n_nodes,
 int build_traj(tree_attn_plan_s* P);
 // The current device if it is a usable sm_103 device.
 int current_device(int* dev);
+// TMA map of a bf16 [rows, heads, d] tensor: boxes of 64 features x 1 head x
+// 128 rows, 128-byte swizzle.
+int make_tensor_map(CUtensorMap* m, const void* base, int64_t rows, int heads, int d);
+// Device address of the current device's status word (kernels' bounded waits).
+int get_status_ptr(int dev, int** out);
 }  // namespace treeattn

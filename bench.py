@@ -16,6 +16,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import math
 import json
 import os
 import statistics
@@ -541,6 +542,31 @@ def run_extras(args):
                       "config": {"workload": "grpo_star logits [11167, 152064] bf16", "predictions": lp.numel(),
                                  "expanded_rows_avoided": int(t.n_expanded - t.n_tokens)}, "dtype": "bf16"}))
     del logits
+
+    # linear attention over the tree (chunks of <= 128 tokens, state handed to children)
+    from prefix_tree_attention_attn_gb300.linear import linear_workspace, tree_linear_fwd
+    for wname in ("grpo_star", "long_context"):
+        tl = WT.load_tree(wname)
+        hl, rl = WX.HEADS[wname], WX.VALUE_RECIPES[wname]
+        xl = WX.draw_inputs(tl.n_tokens, hl, rl, 1000 + WX.SEEDS[wname], device="cuda", chunk_rows=65536)
+        pl = TreePlan(tl.parent, tl.seg_len)
+        nc, wsb = linear_workspace(pl, hl.hkv, hl.d)
+        ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+        dec = torch.full((hl.hkv,), 0.999, dtype=torch.float32, device=dev)
+        ol = torch.empty_like(xl["q"])
+        run = lambda: tree_linear_fwd(pl, xl["q"], xl["k"], xl["v"], dec, 1 / math.sqrt(hl.d), o=ol, workspace=ws)
+        ms = timed(run, iters=10 if wname == "grpo_star" else 3, warm=2)
+        # tensor work issued: per chunk and kv-head K^T V (2 d^2 128), per chunk and
+        # q-head Q K^T, Q S_in and P V (3 x 2 x 128 x 128 x d)
+        flops = nc * (hl.hkv * 2 * hl.d * hl.d * 128 + hl.hq * 3 * 2 * 128 * 128 * hl.d)
+        print(json.dumps({"metric": "tree linear attention forward (chunked, state handoff at branch points)",
+                          "value": tl.n_tokens / (ms / 1e3), "unit": "compact tokens/s", "ms": ms,
+                          "roofline": {"bound": "tensor", "achieved": flops / ms / 1e9, "unit": "TFLOP/s",
+                                       "peak": measured_peaks()[0],
+                                       "frac": flops / ms / 1e9 / measured_peaks()[0]},
+                          "config": {"workload": wname, "chunks": nc, "hq": hl.hq, "hkv": hl.hkv, "d": hl.d,
+                                     "decay": 0.999, "workspace_bytes": wsb}, "dtype": "bf16"}))
+        del xl, ws, ol
 
     ta = WT.load_tree("agentic_tree")
     pa = TreePlan(ta.parent, ta.seg_len)

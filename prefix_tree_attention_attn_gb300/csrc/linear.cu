@@ -11,10 +11,11 @@
 //                     packed order, the entering state of each chunk
 //                     S_in = gamma^L S_in(prev) + dS(prev), a child starting
 //                     from its parent's exit state -- the branch-point handoff;
-//   lin_out_kernel    per (chunk, q-head): S = Q K^T, O = Q S_in (bf16 copy of
-//                     the state as the B operand), then P = S o decay mask
-//                     (registers, written back over S as packed bf16), O rows
-//                     scaled by gamma^(m+1), O += P V; O out as bf16.
+//   lin_out_kernel    per (chunk, kv-head), the group's q-heads in turn:
+//                     S = Q K^T, O = Q S_in (bf16 copy of the state as the B
+//                     operand), then P = S o decay mask (registers, written
+//                     back over S as packed bf16), O rows scaled by
+//                     gamma^(m+1), O += P V; O out as bf16.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -153,11 +154,14 @@ __global__ void __launch_bounds__(256) lin_scan_kernel(const int32_t* __restrict
     }
 }
 
-// ---- outputs per (chunk, q-head) ------------------------------------------------
-// warps 0-3: lane m = query row m of the chunk (and key feature m when staging
-// S_in); warp 4: loads; warp 5: TMEM owner, lane 0 issues the MMAs.
-// TMEM: S / P at columns [0, 128), O at [128, 256).
-constexpr int kOutSmem = 1024 + 4 * kTile;   // Q, K, V, S_in (bf16)
+// ---- outputs per (chunk, kv-head): the group's q-heads one after another ------
+// K, V and the bf16 copy of S_in are loaded once for the G q-heads of the
+// group; Q comes through two slots and TMEM holds two heads (S / P at
+// [256b, 256b + 128), O at [256b + 128, 256b + 256) for buffer b = head & 1), so
+// one head's P and output overlap the next head's S and Q S_in products.
+// warps 0-3: lane m = query row m (and key feature m when staging S_in);
+// warp 4: loads; warp 5: TMEM owner, lane 0 issues the MMAs.
+constexpr int kOutSmem = 1024 + 5 * kTile;   // K, V, S_in (bf16), Q x 2
 
 __global__ void __launch_bounds__(192, 1)
     lin_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -171,68 +175,108 @@ __global__ void __launch_bounds__(192, 1)
         if (threadIdx.x == 0) report_status(status, -5);
         return;
     }
-    const int chunk = blockIdx.x / hq, h = blockIdx.x % hq, g = h / (hq / hkv);
+    const int G = hq / hkv;
+    const int chunk = blockIdx.x / hkv, g = blockIdx.x % hkv;
     const int off = chunks[4 * chunk], L = chunks[4 * chunk + 1];
-    const uint32_t b_full = sb, b_sin = sb + 8, b_s = sb + 16, b_o1 = sb + 24, b_p = sb + 32, b_o2 = sb + 40;
-    const uint32_t holder = sb + 48;
-    const uint32_t qa = sb + 1024, ka = qa + kTile, va = ka + kTile, sina = va + kTile;
+    // barriers: kv, sin, then per buffer b: qfull, qempty, sfull, o1, p, o2, oempty
+    auto bar = [&](int i) { return sb + 8u * (uint32_t)i; };
+    const uint32_t b_kv = bar(0), b_sin = bar(1);
+    auto b_qf = [&](int b) { return bar(2 + b); };
+    auto b_qe = [&](int b) { return bar(4 + b); };
+    auto b_sf = [&](int b) { return bar(6 + b); };
+    auto b_o1 = [&](int b) { return bar(8 + b); };
+    auto b_p = [&](int b) { return bar(10 + b); };
+    auto b_o2 = [&](int b) { return bar(12 + b); };
+    auto b_oe = [&](int b) { return bar(14 + b); };
+    const uint32_t b_drain = bar(16), holder = bar(17);
+    const uint32_t ka = sb + 1024, va = ka + kTile, sina = va + kTile, qa0 = sina + kTile;
     if (threadIdx.x == 0) {
-        mbar_init(b_full, 1);
+        mbar_init(b_kv, 1);
         mbar_init(b_sin, 128);
-        mbar_init(b_s, 1);
-        mbar_init(b_o1, 1);
-        mbar_init(b_p, 128);
-        mbar_init(b_o2, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(b_qf(b), 1);
+            mbar_init(b_qe(b), 1);
+            mbar_init(b_sf(b), 1);
+            mbar_init(b_o1(b), 1);
+            mbar_init(b_p(b), 128);
+            mbar_init(b_o2(b), 1);
+            mbar_init(b_oe(b), 128);
+        }
+        mbar_init(b_drain, 1);
         fence_mbar_init();
     }
-    if (warp == 5) tmem_alloc(holder, 256);
+    if (warp == 5) tmem_alloc(holder, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + 48);
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + 8 * 17);
 
     if (warp == 4) {
         if (lane == 0) {
-            mbar_expect_tx(b_full, 3 * kTile);
+            mbar_expect_tx(b_kv, 2 * kTile);
             for (int blk = 0; blk < 2; ++blk) {
-                tma_load_3d(qa + blk * 16384, &tm_q, blk * 64, h, off, b_full);
-                tma_load_3d(ka + blk * 16384, &tm_k, blk * 64, g, off, b_full);
-                tma_load_3d(va + blk * 16384, &tm_v, blk * 64, g, off, b_full);
+                tma_load_3d(ka + blk * 16384, &tm_k, blk * 64, g, off, b_kv);
+                tma_load_3d(va + blk * 16384, &tm_v, blk * 64, g, off, b_kv);
+            }
+            bool ok = true;
+            for (int n = 0; n < G && ok; ++n) {
+                const int b = n & 1, u = n >> 1;
+                if (u > 0) ok = mbar_wait(b_qe(b), (u - 1) & 1, status, 89);
+                if (!ok) break;
+                mbar_expect_tx(b_qf(b), kTile);
+                for (int blk = 0; blk < 2; ++blk)
+                    tma_load_3d(qa0 + b * kTile + blk * 16384, &tm_q, blk * 64, g * G + n, off, b_qf(b));
             }
         }
     } else if (warp == 5) {
         if (lane == 0) {
             constexpr uint32_t ID_S = idesc_bf16(128, 128, false, false);   // Q K^T
             constexpr uint32_t ID_O = idesc_bf16(128, 128, false, true);    // Q S_in, P V
-            bool ok = mbar_wait(b_full, 0, status, 83);
-            if (ok) {
-                tc_fence_after();
-#pragma unroll
-                for (int k = 0; k < kD / 16; ++k) {
-                    const uint32_t o = (k >> 2) * 16384 + (k & 3) * 32;
-                    mma_bf16_ss(tmem, sdesc_sw128(qa + o, 16, 1024), sdesc_sw128(ka + o, 16, 1024), ID_S, k > 0);
-                }
-                mma_commit(b_s);
-                ok = mbar_wait(b_sin, 0, status, 84);
-            }
-            if (ok) {
-                tc_fence_after();
-#pragma unroll
-                for (int k = 0; k < kD / 16; ++k) {
-                    const uint32_t o = (k >> 2) * 16384 + (k & 3) * 32;
-                    mma_bf16_ss(tmem + 128, sdesc_sw128(qa + o, 16, 1024), sdesc_sw128(sina + k * 2048, 16384, 1024),
-                                ID_O, k > 0);
-                }
-                mma_commit(b_o1);
-                ok = mbar_wait(b_p, 0, status, 85);
-            }
-            if (ok) {
+            bool ok = mbar_wait(b_kv, 0, status, 83);
+            if (ok) ok = mbar_wait(b_sin, 0, status, 84);
+            auto issue_pv = [&](int n) {
+                const int b = n & 1;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < kChunk / 16; ++k)
-                    mma_bf16_ts(tmem + 128, tmem + k * 8, sdesc_sw128(va + k * 2048, 16384, 1024), ID_O, 1u);
-                mma_commit(b_o2);
+                    mma_bf16_ts(tmem + 256 * b + 128, tmem + 256 * b + k * 8, sdesc_sw128(va + k * 2048, 16384, 1024),
+                                ID_O, 1u);
+                mma_commit(b_o2(b));
+            };
+            for (int n = 0; n < G && ok; ++n) {
+                const int b = n & 1, u = n >> 1;
+                if (u > 0) ok = mbar_wait(b_oe(b), (u - 1) & 1, status, 90);   // buffer b read out
+                if (ok) ok = mbar_wait(b_qf(b), u & 1, status, 91);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t qa = qa0 + b * kTile;
+#pragma unroll
+                for (int k = 0; k < kD / 16; ++k) {
+                    const uint32_t o = (k >> 2) * 16384 + (k & 3) * 32;
+                    mma_bf16_ss(tmem + 256 * b, sdesc_sw128(qa + o, 16, 1024), sdesc_sw128(ka + o, 16, 1024), ID_S,
+                                k > 0);
+                }
+                mma_commit(b_sf(b));
+#pragma unroll
+                for (int k = 0; k < kD / 16; ++k) {
+                    const uint32_t o = (k >> 2) * 16384 + (k & 3) * 32;
+                    mma_bf16_ss(tmem + 256 * b + 128, sdesc_sw128(qa + o, 16, 1024),
+                                sdesc_sw128(sina + k * 2048, 16384, 1024), ID_O, k > 0);
+                }
+                mma_commit(b_o1(b));
+                mma_commit(b_qe(b));   // Q slot b is no longer read
+                if (n > 0) {           // the previous head's P V
+                    ok = mbar_wait(b_p((n - 1) & 1), ((n - 1) >> 1) & 1, status, 85);
+                    if (!ok) break;
+                    issue_pv(n - 1);
+                }
             }
+            if (ok) {
+                ok = mbar_wait(b_p((G - 1) & 1), ((G - 1) >> 1) & 1, status, 92);
+                if (ok) issue_pv(G - 1);
+            }
+            mma_commit(b_drain);
+            mbar_wait(b_drain, 0, status, 93);
         }
         __syncwarp();
     } else {
@@ -245,76 +289,83 @@ __global__ void __launch_bounds__(192, 1)
             const float4* src = reinterpret_cast<const float4*>(s_in + (((size_t)chunk * hkv + g) * kD + m) * kD);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {   // 8 features per 16-byte chunk
-                const float4 a = src[2 * j], b = src[2 * j + 1];
+                const float4 a4 = src[2 * j], b4 = src[2 * j + 1];
                 const int blk = j >> 3, cj = j & 7;
-                st_shared_v4(sina + blk * 16384 + sw128_offset(m, cj), pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w),
-                             pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
+                st_shared_v4(sina + blk * 16384 + sw128_offset(m, cj), pack_bf16x2(a4.x, a4.y),
+                             pack_bf16x2(a4.z, a4.w), pack_bf16x2(b4.x, b4.y), pack_bf16x2(b4.z, b4.w));
             }
             fence_proxy_async_smem();
             mbar_arrive(b_sin);
         }
-        bool ok = mbar_wait(b_s, 0, status, 86);
-        ok = __all_sync(0xffffffffu, ok);
-        if (ok) {
-            tc_fence_after();
-            // P[m, m'] = scale * S[m, m'] * gamma^(m - m') for m' <= m and m' < L
+        const float fo = scale * exp2f((float)(m + 1) * lg);   // weight of the carried-in part
+        bool ok = true;
+        for (int n = 0; n < G; ++n) {
+            const int b = n & 1, u = n >> 1, h = g * G + n;
+            const uint32_t tS = lane_base + 256 * b, tO = tS + 128;
+            if (ok) ok = mbar_wait(b_sf(b), u & 1, status, 86);
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok) {
+                tc_fence_after();
+                // P[m, m'] = scale * S[m, m'] * gamma^(m - m') for m' <= m and m' < L
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                float v[32];
-                tmem_ld32(lane_base + cc * 32, v);
-                tmem_wait_ld();
-                uint32_t pw[16];
+                for (int cc = 0; cc < 4; ++cc) {
+                    float v[32];
+                    tmem_ld32(tS + cc * 32, v);
+                    tmem_wait_ld();
+                    uint32_t pw[16];
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const int c0 = cc * 32 + 2 * u, c1 = c0 + 1;
-                    const float p0 = (c0 <= m && c0 < L) ? scale * v[2 * u] * exp2f((float)(m - c0) * lg) : 0.f;
-                    const float p1 = (c1 <= m && c1 < L) ? scale * v[2 * u + 1] * exp2f((float)(m - c1) * lg) : 0.f;
-                    pw[u] = pack_bf16x2(p0, p1);
+                    for (int w = 0; w < 16; ++w) {
+                        const int c0 = cc * 32 + 2 * w, c1 = c0 + 1;
+                        const float p0 = (c0 <= m && c0 < L) ? scale * v[2 * w] * exp2f((float)(m - c0) * lg) : 0.f;
+                        const float p1 =
+                            (c1 <= m && c1 < L) ? scale * v[2 * w + 1] * exp2f((float)(m - c1) * lg) : 0.f;
+                        pw[w] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st16(tS + cc * 16, pw);
                 }
-                tmem_st16(lane_base + cc * 16, pw);
+                tmem_wait_st();
+                ok = mbar_wait(b_o1(b), u & 1, status, 87);
             }
-            tmem_wait_st();
-            ok = mbar_wait(b_o1, 0, status, 87);
-        }
-        ok = __all_sync(0xffffffffu, ok);
-        if (ok) {
-            tc_fence_after();
-            // the carried-in part: scale * gamma^(m+1) * (q_m . S_in)
-            const float f = scale * exp2f((float)(m + 1) * lg);
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok) {
+                tc_fence_after();
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                float v[32];
-                tmem_ld32(lane_base + 128 + cc * 32, v);
-                tmem_wait_ld();
+                for (int cc = 0; cc < 4; ++cc) {
+                    float v[32];
+                    tmem_ld32(tO + cc * 32, v);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int u = 0; u < 32; ++u) v[u] *= f;
-                tmem_st32(lane_base + 128 + cc * 32, v);
+                    for (int w = 0; w < 32; ++w) v[w] *= fo;
+                    tmem_st32(tO + cc * 32, v);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(b_p(b));
+                ok = mbar_wait(b_o2(b), u & 1, status, 88);
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(b_p);
-            ok = mbar_wait(b_o2, 0, status, 88);
-        }
-        ok = __all_sync(0xffffffffu, ok);
-        if (ok) {
-            tc_fence_after();
-            uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)(off + m) * hq + h) * kD);
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok) {
+                tc_fence_after();
+                uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)(off + m) * hq + h) * kD);
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                float v[32];
-                tmem_ld32(lane_base + 128 + cc * 32, v);
-                tmem_wait_ld();
-                if (m < L) {
+                for (int cc = 0; cc < 4; ++cc) {
+                    float v[32];
+                    tmem_ld32(tO + cc * 32, v);
+                    tmem_wait_ld();
+                    if (m < L) {
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        uint4 w;
-                        w.x = pack_bf16x2(v[8 * u], v[8 * u + 1]);
-                        w.y = pack_bf16x2(v[8 * u + 2], v[8 * u + 3]);
-                        w.z = pack_bf16x2(v[8 * u + 4], v[8 * u + 5]);
-                        w.w = pack_bf16x2(v[8 * u + 6], v[8 * u + 7]);
-                        dst[cc * 4 + u] = w;
+                        for (int w = 0; w < 4; ++w) {
+                            uint4 x;
+                            x.x = pack_bf16x2(v[8 * w], v[8 * w + 1]);
+                            x.y = pack_bf16x2(v[8 * w + 2], v[8 * w + 3]);
+                            x.z = pack_bf16x2(v[8 * w + 4], v[8 * w + 5]);
+                            x.w = pack_bf16x2(v[8 * w + 6], v[8 * w + 7]);
+                            dst[cc * 4 + w] = x;
+                        }
                     }
                 }
+                tc_fence_before();
+                mbar_arrive(b_oe(b));   // buffer b may take the head after next
             }
         }
     }
@@ -322,7 +373,7 @@ __global__ void __launch_bounds__(192, 1)
     __syncthreads();
     if (warp == 5) {
         tc_fence_after();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, 512);
     }
 }
 
@@ -459,7 +510,7 @@ int tree_attn_linear_fwd(tree_attn_plan_t P, const void* q, const void* k, const
     lin_scan_kernel<<<dim3(kD * kD / 256, hkv), 256, 0, s>>>(D->lnodes, P->n_nodes, D->chunks, decay, hkv, ds, s_in,
                                                              s_out);
     if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
-    lin_out_kernel<<<(unsigned)(nc * hq), 192, kOutSmem, s>>>(tq, tk, tv, D->chunks, decay, s_in,
+    lin_out_kernel<<<(unsigned)(nc * hkv), 192, kOutSmem, s>>>(tq, tk, tv, D->chunks, decay, s_in,
                                                               static_cast<uint16_t*>(o), hq, hkv, scale, status);
     return cudaGetLastError() == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
 }

@@ -55,7 +55,10 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the CPU sample")
     ap.add_argument("--extras", action="store_true",
                     help="instead of the step, time the calls around it (tree batching, loss boundary, "
-                         "subtree advantages); one JSON line each")
+                         "subtree advantages, tree linear attention); one JSON line each")
+    ap.add_argument("--extras-small", action="store_true",
+                    help="with --extras: GRPO star only and a 32,768-token vocabulary (a few GB on the device, "
+                         "for profiler captures)")
     return ap.parse_args()
 
 
@@ -530,7 +533,7 @@ def run_extras(args):
                       "unit": "GB/s", "ms": ms, "roofline": {"bound": "hbm", "peak": hbm, "frac": nbytes / ms / 1e6 / hbm},
                       "config": {"workload": "grpo_star dO [11167, 32, 128] bf16"}, "dtype": "bf16"}))
 
-    V = 152064
+    V = 32768 if args.extras_small else 152064
     g = torch.Generator(device="cuda").manual_seed(9)
     logits = (torch.randn(t.n_tokens, V, generator=g, device=dev) * 2.0).to(torch.bfloat16)
     tokens = torch.randint(0, V, (t.n_tokens,), generator=g, device=dev, dtype=torch.int32)
@@ -539,13 +542,13 @@ def run_extras(args):
     nbytes = logits.numel() * 2 + lp.numel() * (4 + 8 + 4 + 2) + t.n_tokens * 4
     print(json.dumps({"metric": "per-trajectory next-token log-probs from compact logits", "value": nbytes / ms / 1e6,
                       "unit": "GB/s", "ms": ms, "roofline": {"bound": "hbm", "peak": hbm, "frac": nbytes / ms / 1e6 / hbm},
-                      "config": {"workload": "grpo_star logits [11167, 152064] bf16", "predictions": lp.numel(),
+                      "config": {"workload": f"grpo_star logits [11167, {V}] bf16", "predictions": lp.numel(),
                                  "expanded_rows_avoided": int(t.n_expanded - t.n_tokens)}, "dtype": "bf16"}))
     del logits
 
     # linear attention over the tree (chunks of <= 128 tokens, state handed to children)
     from prefix_tree_attention_attn_gb300.linear import linear_workspace, tree_linear_fwd
-    for wname in ("grpo_star", "long_context"):
+    for wname in ("grpo_star",) if args.extras_small else ("grpo_star", "long_context"):
         tl = WT.load_tree(wname)
         hl, rl = WX.HEADS[wname], WX.VALUE_RECIPES[wname]
         xl = WX.draw_inputs(tl.n_tokens, hl, rl, 1000 + WX.SEEDS[wname], device="cuda", chunk_rows=65536)

@@ -182,7 +182,28 @@ def cpu_baseline(tree, x, heads, scale, target_s):
     dt = time.perf_counter() - t0
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"fp64 numpy oracle, fwd+bwd of {groups} of {heads.hkv} kv-head groups "
-                      f"({groups * heads.group} q-heads) of the full tree, {dt:.1f} s; numpy BLAS default threads"}
+                      f"({groups * heads.group} q-heads) of the full tree, {dt:.1f} s; numpy BLAS default threads",
+            "cpu_model": cpu_model(), "blas_threads": blas_threads()}
+
+
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu part", "hardware"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def blas_threads():
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return os.cpu_count()
 
 
 def run_reference(args):
@@ -264,6 +285,10 @@ def run_ours(args):
     tree = WT.load_tree(args.workload)
     heads, rec, x = WX.workload_inputs(args.workload, tree.n_tokens)
     hq, hkv, d, scale = heads.hq, heads.hkv, heads.d, rec.scale
+    t_plan = time.perf_counter()
+    for _ in range(5):
+        TA.TreePlan(tree.parent, tree.seg_len).close()
+    plan_ms = (time.perf_counter() - t_plan) * 1e3 / 5   # host planner, reported on its own
     plan = TA.TreePlan(tree.parent, tree.seg_len)
     N = plan.n_tokens
     f_fwd, f_bwd = useful_flops(plan.n_pairs, hq, d)
@@ -441,6 +466,8 @@ def run_ours(args):
                        "softmax_scale": scale, "l2": "flushed between timed steps (512 MB write, untimed)",
                        "parallelism": f"replicas x{world} (independent trees per GPU)"},
             "pct_peak": 100.0 * value / world / peak_burst,
+            "ms_per_step_median": statistics.median(step_ms),
+            "plan_ms_host": plan_ms,
             "fwd_ms": fwd_ms, "bwd_pre_ms": pre_ms, "bwd_main_ms": main_ms, "bwd_post_ms": post_ms,
             "fwd_tflops": f_fwd / (fwd_ms / 1e3) / 1e12, "bwd_main_tflops": f_bwd / (main_ms / 1e3) / 1e12,
             "roofline": roofline,
@@ -506,7 +533,7 @@ def run_extras(args):
     dev = torch.device("cuda:0")
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
-    def timed(fn, iters=20, warm=3):
+    def timed_steps(fn, iters, warm):
         for _ in range(warm):
             fn()
         ms = []
@@ -519,6 +546,32 @@ def run_extras(args):
             torch.cuda.synchronize()
             ms.append(e0.elapsed_time(e1))
         return statistics.median(ms)
+
+    # the tiny binary tree is latency-bound alone (one launch for 3.9e7 FLOP); 4,096 copies
+    # packed as one forest by the batching calls run in one fwd + bwd call
+    tiny = WT.load_tree("tiny_binary")
+    copies = 4096
+    fpar, fseg, _ = TB.TreeBatch([(tiny.parent, tiny.seg_len)] * copies).forest([True] * copies)
+    fplan = TreePlan(fpar, fseg)
+    th, trc = WX.HEADS["tiny_binary"], WX.VALUE_RECIPES["tiny_binary"]
+    tx = WX.draw_inputs(fplan.n_tokens, th, trc, 1000 + WX.SEEDS["tiny_binary"], device="cuda")
+    from prefix_tree_attention_attn_gb300 import tree_attn_bwd, tree_attn_fwd
+
+    def tiny_step():
+        o_, l_ = tree_attn_fwd(fplan, tx["q"], tx["k"], tx["v"], trc.scale)
+        tree_attn_bwd(fplan, tx["q"], tx["k"], tx["v"], o_, l_, tx["do"], trc.scale)
+
+    ms = timed_steps(tiny_step, 10, 3)
+    ff, fb = useful_flops(fplan.n_pairs, th.hq, th.d)
+    print(json.dumps({"metric": METRIC + " (variant: tiny binary tree x 4096 as one forest)",
+                      "value": (ff + fb) / (ms / 1e3) / 1e12, "unit": UNIT, "ms": ms,
+                      "pct_peak": 100 * (ff + fb) / (ms / 1e3) / 1e12 / measured_peaks()[0],
+                      "config": {"workload": "tiny_binary x 4096 forest", "n_tokens": fplan.n_tokens,
+                                 "pairs": fplan.n_pairs, "hq": th.hq, "hkv": th.hkv, "d": th.d}, "dtype": "bf16"}))
+    del tx
+
+    def timed(fn, iters=20, warm=3):
+        return timed_steps(fn, iters, warm)
 
     t = WT.load_tree("grpo_star")
     heads, rec = WX.HEADS["grpo_star"], WX.VALUE_RECIPES["grpo_star"]

@@ -215,20 +215,38 @@ __global__ void __launch_bounds__(FwdCfg<D, NS>::NWARPS * 32, 1)
         const float sl2 = p.scale_log2;
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
+        // The tile list, this row's subtree end of each partial tile's keys and the
+        // tile's minimum subtree end are loaded a tile ahead (the list entry two
+        // ahead), so no global-memory latency sits on a tile's critical path.
+        int ent_next = p.qt_ent[e0];
+        int sub_next = 0, min_next = 0;
+        if (ent_next & 1) {
+            sub_next = p.subend[(ent_next >> 1) * 128 + r];
+            min_next = p.kv_minsub[ent_next >> 1];
+        }
+        int ent_after = n_kv > 1 ? p.qt_ent[e0 + 1] : 0;
         for (int j = 0; j < n_kv; ++j) {
-            const int ent = p.qt_ent[e0 + j];
+            const int ent = ent_next;
             const int c = ent >> 1;
             const bool partial = ent & 1;
-            int my_sub = 0;
-            if (partial) my_sub = p.subend[c * 128 + r];
+            const int my_sub = sub_next, kv_min = min_next;
+            ent_next = ent_after;
+            if (j + 1 < n_kv && (ent_next & 1)) {
+                sub_next = p.subend[(ent_next >> 1) * 128 + r];
+                min_next = p.kv_minsub[ent_next >> 1];
+            }
+            if (j + 2 < n_kv) ent_after = p.qt_ent[e0 + j + 2];
             // After a failed wait the loop keeps running (work skipped) so that every
             // thread of the group meets the same named barriers in the same order.
             if (ok) ok = mbar_wait(b_sfull(s), j & 1, p.status, 8);
             ok = __all_sync(0xffffffffu, ok);
+            // One barrier publishes the staged subtree ends and makes `ok` uniform.
+            // Overwriting the staging row is safe without a barrier before it: S of
+            // this tile exists only after every thread of the group has arrived on
+            // the previous tile's P barrier, i.e. finished reading the old values.
             if (partial) {
-                ok = named_bar_and(1 + s, 128, ok);
                 if (ok) sub_sm[r] = my_sub;
-                named_bar_sync(1 + s, 128);
+                ok = named_bar_and(1 + s, 128, ok);
             }
             if (!ok) continue;
             tc_fence_after();
@@ -238,7 +256,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NS>::NWARPS * 32, 1)
             // TMEM, so pass 2 never masks.
             const int kbase = c * 128;
             const bool need_mask =
-                partial && !__all_sync(0xffffffffu, kbase + 127 <= i && i < p.kv_minsub[c]);
+                partial && !__all_sync(0xffffffffu, kbase + 127 <= i && i < kv_min);
             auto mask = [&](float (&v)[32], int cc) {
 #pragma unroll
                 for (int u4 = 0; u4 < 8; ++u4) {

@@ -21,6 +21,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -107,7 +108,9 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{index}.csv")
+        # raw samples go to BENCH_OUT_DIR (default: a temporary directory)
+        out = os.environ.get("BENCH_OUT_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(out, f"clocks_bench_{index}.csv")
 
     def start(self):
         try:

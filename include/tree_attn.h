@@ -2,16 +2,15 @@
  * tree_attn.h -- C ABI of libtreeattn: causal softmax attention over a packed
  * rollout prefix tree, forward and backward, on one GB300 (sm_103a).
  *
- * What it computes.  RL rollouts share long prefixes and form a tree
- * (AReaL-DTA abstract; HARTS abstract: "irregular rollout trees with shared
- * histories").  Each shared prefix is stored once: the compact token sequence
+ * What it computes.  RL rollouts share long prefixes and form a tree, often an
+ * irregular one (AReaL-DTA abstract; HARTS abstract).  Each shared prefix is
+ * stored once: the compact token sequence
  * lists the node segments in depth-first pre-order (roots, then children, in
  * ascending node id).  Query token i attends to key token j exactly when j
  * lies on i's root-to-node path and, inside i's own segment, j <= i.  So every
  * token gets the output and the gradients that training its root-to-leaf
- * trajectory on its own would give -- the equivalence both abstracts ask for
- * ("Training root-to-leaf trajectories independently recomputes these shared
- * prefixes"), without recomputing the prefixes.
+ * trajectory on its own would give -- the equivalence both abstracts ask for --
+ * while each shared prefix is computed once instead of once per trajectory.
  *
  *   S_ij = softmax_scale * q_i . k_j            (attended pairs only)
  *   LSE_i = ln sum_j exp(S_ij),   P_ij = exp(S_ij - LSE_i),   O_i = sum_j P_ij v_j

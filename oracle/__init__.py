@@ -6,10 +6,9 @@ with it: the GPU path has its own planner (C++) and kernels (CUDA).
 
 What it computes (the equivalence the pages require): every token of a rollout
 prefix tree must get the output and gradients it would get if its root-to-leaf
-trajectory were trained on its own (AReaL-DTA abstract: independent processing
-"repeatedly recomput[es] identical prefixes in both the forward and backward
-passes"; HARTS abstract: "Training root-to-leaf trajectories independently
-recomputes these shared prefixes").  So the oracle expands every trajectory,
+trajectory were trained on its own (AReaL-DTA abstract and HARTS abstract:
+separate training of each trajectory computes the shared prefixes again for
+every trajectory, forward and backward).  So the oracle expands every trajectory,
 runs plain dense causal softmax attention on it in fp64, and maps the results
 back onto the compact tokens.
 

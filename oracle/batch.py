@@ -2,7 +2,7 @@
 
 Follows the definitions the batching calls state (AReaL-DTA abstract: trees
 assigned to GPUs to balance work; HARTS abstract: microbatches and replica
-assignments planned from compact-token work), with this build's readings:
+assignments planned from compact-token work), with these readings of ours:
 
 * work of a tree = its ancestor pairs: the number of (query, key) token pairs
   with the key on the query's root-to-node path (inside the query's own segment:

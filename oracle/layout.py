@@ -2,9 +2,9 @@
 
 Packing convention (the data format shared with the library's callers): the
 compact token sequence lists node segments in depth-first pre-order, roots in
-ascending node id, children of a node in ascending node id.  The pages fix the
-DFS traversal (AReaL-DTA abstract: "depth-first search (DFS)-based execution
-strategy"); the sibling order is this build's reading (ascending id).
+ascending node id, children of a node in ascending node id.  The pages fix a
+depth-first traversal of the tree (AReaL-DTA abstract); the sibling order is
+a reading of ours (ascending id).
 
 Everything here walks parent pointers; nothing uses the library's planner.
 """

@@ -3,7 +3,7 @@ infrastructure).
 
 HARTS (abstract): hybrid models mix softmax attention with linear attention,
 whose recurrent state must be carried from a shared prefix into every branch.
-This build's reading (the pages give no formula): per q-head h with kv-head
+Our reading (the pages give no formula): per q-head h with kv-head
 g = h // G and a per-kv-head decay gamma_g in (0, 1],
 
     o_i = scale * sum_{j on i's root-to-node path, j <= i} gamma^(pos_i - pos_j) (q_i . k_j) v_j

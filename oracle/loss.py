@@ -12,7 +12,7 @@ parent pointers; fp64 throughout.
   per-trajectory log-probs is the step that precedes the loss);
 * subtree advantages (TreePO: advantages over sub-trees from collective
   descendant outcomes; simple vs size-weighted subgroup aggregation; the root
-  group optional).  This build's reading, written out in the library header:
+  group optional).  Our reading, written out in the library header:
   subgroups of leaf l = nodes u on its root path with at least two leaves below;
   a_u(l) = R_l - mean_u, optionally / (std_u + eps) (population std); A(l) the
   plain or |G(u)|-weighted mean of a_u(l); node coefficient = sum of A over the

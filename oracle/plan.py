@@ -20,9 +20,9 @@ T = ceil(N / B) tiles):
   index >= N are not valid and are ignored.
 * ``kv_range[c]`` -- half-open range of q-tiles with a non-empty (t, c) block.
 
-The pages ask for key intervals and full / partial / empty tiles per query tile
-(the packed tree-mask family that the AReaL-DTA abstract says "scale[s]
-poorly" -- tile skipping removes the quadratic mask scan).
+The plan lists key intervals and full / partial / empty tiles per query tile:
+the AReaL-DTA abstract faults packed tree-mask methods for poor scaling, and
+skipping empty tiles removes the quadratic mask scan.
 """
 from __future__ import annotations
 

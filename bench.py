@@ -423,20 +423,47 @@ def run_ours(args):
                            "backward (side stream)"}
 
     # ---- same kernels on the expanded trajectories ---------------------------
+    # Every root-to-leaf trajectory as its own chain. When the whole expanded
+    # forest does not fit in half of the free device memory (the long shared
+    # context: ~2.6 M tokens), the chains run in equal batches one after another
+    # inside each timed step, and the step time is the sum.
     expanded = None
     if not args.no_expanded and rank == 0:
         ft = WT.expanded_forest(tree)
-        fp = TA.TreePlan(ft.parent, ft.seg_len)
-        Ne = fp.n_tokens
+        lens = list(ft.seg_len)
+        n_leaves = len(lens)
+
+        def batch_bytes(ls):
+            pb = TA.TreePlan([-1] * len(ls), ls)
+            nt = pb.n_tokens
+            ws = pb.workspace_size(hq, hkv, d)[1]
+            pb.close()
+            return nt * (4 * hq + 4 * hkv) * d * 2 + 4 * hq * nt + ws
+
+        free_b = torch.cuda.mem_get_info(dev)[0]
+        n_batches = 1
+        while True:
+            per = -(-n_leaves // n_batches)
+            groups = [lens[i:i + per] for i in range(0, n_leaves, per)]
+            if max(batch_bytes(gl) for gl in groups) <= 0.5 * free_b or per == 1:
+                break
+            n_batches *= 2
+        eplans = [TA.TreePlan([-1] * len(gl), gl) for gl in groups]
+        Ne = sum(pb.n_tokens for pb in eplans)
+        Nmax = max(pb.n_tokens for pb in eplans)
         g = torch.Generator(device=dev)
         g.manual_seed(7)
-        xe = {n: (torch.randn((Ne, h, d), generator=g, device=dev, dtype=torch.float32)).to(torch.bfloat16)
+        xe = {n: (torch.randn((Nmax, h, d), generator=g, device=dev, dtype=torch.float32)).to(torch.bfloat16)
               for n, h in (("q", hq), ("k", hkv), ("v", hkv), ("do", hq))}
-        wse = torch.empty(max(fp.workspace_size(hq, hkv, d)[1], 1), dtype=torch.uint8, device=dev)
+        wse = torch.empty(max(max(pb.workspace_size(hq, hkv, d)[1] for pb in eplans), 1), dtype=torch.uint8,
+                          device=dev)
 
         def estep():
-            oo, ll = TA.tree_attn_fwd(fp, xe["q"], xe["k"], xe["v"], scale)
-            TA.tree_attn_bwd(fp, xe["q"], xe["k"], xe["v"], oo, ll, xe["do"], scale, workspace=wse)
+            for pb in eplans:
+                nb = pb.n_tokens
+                qb, kb, vb, dob = (xe[n][:nb] for n in ("q", "k", "v", "do"))
+                oo, ll = TA.tree_attn_fwd(pb, qb, kb, vb, scale)
+                TA.tree_attn_bwd(pb, qb, kb, vb, oo, ll, dob, scale, workspace=wse)
 
         for _ in range(3):
             estep()
@@ -452,7 +479,10 @@ def run_ours(args):
         torch.cuda.synchronize()
         ems = statistics.mean(a_.elapsed_time(b_) for a_, b_ in ee)
         expanded = {"ms_per_step": ems, "speedup": ems / (total_ms / args.steps), "n_tokens": Ne,
-                    "pairs": fp.n_pairs}
+                    "pairs": sum(pb.n_pairs for pb in eplans), "chain_batches": len(eplans)}
+        for pb in eplans:
+            pb.close()
+        del xe, wse
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

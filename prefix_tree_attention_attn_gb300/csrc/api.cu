@@ -19,6 +19,8 @@ __device__ int g_device_status = 0;
 namespace {
 
 constexpr int kBlock = 128;
+// mean kv-tiles per q-tile up to which the forward runs one q-head per CTA, two CTAs per SM
+constexpr int kFwdShortList = 24;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -295,7 +297,12 @@ int tree_attn_fwd(tree_attn_plan_t P, const void* q, const void* k, const void* 
         (st = make_tmap(&tv, v, P->N, hkv, d)) || (st = make_tmap(&to, o, P->N, hq, d)))
         return st;
     const int group = hq / hkv;
-    const int ns = (group % 2 == 0) ? 2 : 1;
+    // Short kv-tile lists (at most 24 per q-tile on average): one q-head per CTA,
+    // two CTAs per SM, so CTA prologues and epilogues overlap other CTAs' tiles.
+    // Longer lists: two q-heads per CTA share every K/V tile (even group size).
+    const bool short_lists = (int64_t)P->qt_kv.size() <= kFwdShortList * (int64_t)P->T;
+    const int ns = (!short_lists && group % 2 == 0) ? 2 : 1;
+    const int per_sm = short_lists ? 2 : 1;
     FwdParams p;
     p.qt_ptr = D->qt_ptr;
     p.qt_ent = D->qt_ent;
@@ -311,7 +318,7 @@ int tree_attn_fwd(tree_attn_plan_t P, const void* q, const void* k, const void* 
     cudaGetDevice(&dev);
     if ((st = status_ptr(dev, &p.status))) return st;
     const int grid = P->T * (hq / ns);
-    cudaError_t e = launch_fwd(d, ns, &tq, &tk, &tv, &to, p, grid, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_fwd(d, ns, per_sm, &tq, &tk, &tv, &to, p, grid, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
 }
 

@@ -1,10 +1,18 @@
 // Forward kernel: O and LSE of causal softmax attention over a packed prefix
 // tree, on the sm_103a tensor cores.
 //
-// One CTA = one 128-row q-tile x NS q-heads of the same kv-head group (NS = 2
-// when the group size is even).  The two q-heads read the same key tiles, so
-// every K/V tile is loaded once for both.  The CTA visits only the kv-tiles in
-// the q-tile's ancestor interval list; empty tiles are never loaded.
+// One CTA = one 128-row q-tile x NS q-heads of the same kv-head group.  The CTA
+// visits only the kv-tiles in the q-tile's ancestor interval list; empty tiles
+// are never loaded.  Two shapes:
+//  * NS = 2 (even group size, long kv-tile lists): the two q-heads read the same
+//    key tiles, so every K/V tile is loaded once for both; one CTA per SM with a
+//    deep K/V ring.
+//  * NS = 1, two CTAs per SM (short lists): a 2-slot ring and 256 TMEM columns
+//    per CTA, so two CTAs share an SM and one CTA's prologue (Q and first K
+//    load, first S) and epilogue overlap the other's tiles.  With a handful of
+//    kv-tiles per q-tile that overlap is worth more than loading each K/V tile
+//    once per head pair.
+//  * NS = 1, one CTA per SM: long lists with an odd group size.
 //
 // Warp roles (NS = 2; 320 threads):
 //   warps 0-3  softmax for q-head 0 (one query row per thread)
@@ -36,12 +44,15 @@ namespace treeattn {
 
 namespace {
 
-template <int D, int NS>
+template <int D, int NS, int PER_SM>
 struct FwdCfg {
+    static_assert(PER_SM == 1 || NS == 1, "two CTAs per SM only with one q-head per CTA");
     static constexpr int TILE = 128 * D * 2;          // Q/K/V tile bytes
     static constexpr int SMALL = 3072;                // barriers + subend staging
     // K/V ring: every slot that fits next to Q (at most 8)
-    static constexpr int NSLOT = (229376 - NS * TILE) / TILE < 8 ? (229376 - NS * TILE) / TILE : 8;
+    // (two CTAs per SM: 2 slots, 101 KB per CTA)
+    static constexpr int NSLOT =
+        PER_SM == 2 ? 2 : ((229376 - NS * TILE) / TILE < 8 ? (229376 - NS * TILE) / TILE : 8);
     static constexpr int OFF_Q = SMALL;
     static constexpr int OFF_KV = OFF_Q + NS * TILE;
     static constexpr int BYTES = OFF_KV + NSLOT * TILE;
@@ -62,17 +73,18 @@ struct FwdCfg {
     static_assert(SUB + NS * 512 <= SMALL, "small region");
     static_assert(HOLDER + 4 <= SUB, "barriers");
     static_assert(BYTES <= 232448, "shared memory");
-    static_assert(NSLOT >= NS && NSLOT >= 3, "the epilogue stages O in ring slots");
+    static_assert(NSLOT >= NS && NSLOT >= 2, "the epilogue stages O in ring slots");
+    static_assert(PER_SM * BYTES <= 232448, "CTAs per SM");
 };
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
 
-template <int D, int NS>
-__global__ void __launch_bounds__(FwdCfg<D, NS>::NWARPS * 32, 1)
+template <int D, int NS, int PER_SM>
+__global__ void __launch_bounds__(FwdCfg<D, NS, PER_SM>::NWARPS * 32, PER_SM)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                const FwdParams p) {
-    using C = FwdCfg<D, NS>;
+    using C = FwdCfg<D, NS, PER_SM>;
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sb = smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -369,11 +381,11 @@ __global__ void __launch_bounds__(FwdCfg<D, NS>::NWARPS * 32, 1)
     }
 }
 
-template <int D, int NS>
+template <int D, int NS, int PER_SM>
 cudaError_t launch_cfg(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv, const CUtensorMap* to,
                        const FwdParams& p, int grid, cudaStream_t stream) {
-    using C = FwdCfg<D, NS>;
-    auto kern = fwd_kernel<D, NS>;
+    using C = FwdCfg<D, NS, PER_SM>;
+    auto kern = fwd_kernel<D, NS, PER_SM>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES);
     if (e != cudaSuccess) return e;
     kern<<<grid, C::NWARPS * 32, C::BYTES, stream>>>(*tq, *tk, *tv, *to, p);
@@ -382,12 +394,17 @@ cudaError_t launch_cfg(const CUtensorMap* tq, const CUtensorMap* tk, const CUten
 
 }  // namespace
 
-cudaError_t launch_fwd(int d, int nstream, const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
-                       const CUtensorMap* to, const FwdParams& p, int grid, cudaStream_t stream) {
-    if (d == 128) return nstream == 2 ? launch_cfg<128, 2>(tq, tk, tv, to, p, grid, stream)
-                                      : launch_cfg<128, 1>(tq, tk, tv, to, p, grid, stream);
-    return nstream == 2 ? launch_cfg<64, 2>(tq, tk, tv, to, p, grid, stream)
-                        : launch_cfg<64, 1>(tq, tk, tv, to, p, grid, stream);
+cudaError_t launch_fwd(int d, int nstream, int per_sm, const CUtensorMap* tq, const CUtensorMap* tk,
+                       const CUtensorMap* tv, const CUtensorMap* to, const FwdParams& p, int grid,
+                       cudaStream_t stream) {
+    if (d == 128) {
+        if (nstream == 2) return launch_cfg<128, 2, 1>(tq, tk, tv, to, p, grid, stream);
+        return per_sm == 2 ? launch_cfg<128, 1, 2>(tq, tk, tv, to, p, grid, stream)
+                           : launch_cfg<128, 1, 1>(tq, tk, tv, to, p, grid, stream);
+    }
+    if (nstream == 2) return launch_cfg<64, 2, 1>(tq, tk, tv, to, p, grid, stream);
+    return per_sm == 2 ? launch_cfg<64, 1, 2>(tq, tk, tv, to, p, grid, stream)
+                       : launch_cfg<64, 1, 1>(tq, tk, tv, to, p, grid, stream);
 }
 
 }  // namespace treeattn

@@ -56,8 +56,10 @@ struct BwdPostParams {
 };
 
 // Launchers return cudaSuccess or the launch error.
-cudaError_t launch_fwd(int d, int nstream, const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
-                       const CUtensorMap* to, const FwdParams& p, int grid, cudaStream_t stream);
+// nstream q-heads per CTA; per_sm = 2 (only with nstream = 1): the two-CTAs-per-SM shape
+cudaError_t launch_fwd(int d, int nstream, int per_sm, const CUtensorMap* tq, const CUtensorMap* tk,
+                       const CUtensorMap* tv, const CUtensorMap* to, const FwdParams& p, int grid,
+                       cudaStream_t stream);
 cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t stream);
 cudaError_t launch_bwd(int d, const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                        const CUtensorMap* tdo, const CUtensorMap* tdq, const BwdParams& p, int grid,

@@ -59,6 +59,21 @@ def test_random_trees(seed):
     full_parity(t, q, k, v, do, 1 / np.sqrt(d), tag=f"seed{seed}")
 
 
+@pytest.mark.parametrize("heads", [(4, 2, 128), (3, 1, 128)])
+def test_long_kv_lists(heads):
+    """A tree whose q-tiles see more than 24 kv-tiles on average: the forward
+    then runs its long-list shapes (two q-heads per CTA for an even group size,
+    one q-head per CTA with a deep ring for an odd one) instead of the
+    two-CTAs-per-SM shape the other cases use."""
+    t = WT.Tree("long_lists", [-1, 0, 0], [6400, 700, 900])
+    plan = TreePlan(t.parent, t.seg_len)
+    ex = plan.export(("qt_ptr",))
+    assert (len(ex["qt_ptr"]) - 1) * 24 < ex["qt_ptr"][-1]
+    hq, hkv, d = heads
+    q, k, v, do = draw(t.n_tokens, hq, hkv, d, seed=31 + hq)
+    full_parity(t, q, k, v, do, 1 / np.sqrt(d), tag=f"long_lists_{hq}_{hkv}")
+
+
 def test_sharp_logits():
     """Unscaled N(0,1) q/k with a large softmax scale: peaked rows, which
     exercise the O rescaling when the running maximum jumps."""

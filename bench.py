@@ -263,6 +263,27 @@ def job_throughput(flops_per_step: float, steps: int, world: int, max_ms: float)
     return flops_per_step * steps * world / (max_ms / 1e3) / 1e12
 
 
+def chain_batches(TA, lens, hq, hkv, d, budget_bytes):
+    """Split chains (token counts `lens`, in order) into equal contiguous
+    batches, doubling the batch count until one batch's device bytes (Q, K, V,
+    dO, O, dQ, dK, dV in bf16, LSE, backward workspace) fit in budget_bytes,
+    or every batch holds one chain."""
+    def batch_bytes(ls):
+        pb = TA.TreePlan([-1] * len(ls), ls)
+        nt = pb.n_tokens
+        ws = pb.workspace_size(hq, hkv, d)[1]
+        pb.close()
+        return nt * (4 * hq + 4 * hkv) * d * 2 + 4 * hq * nt + ws
+
+    n_batches = 1
+    while True:
+        per = -(-len(lens) // n_batches)
+        groups = [lens[i:i + per] for i in range(0, len(lens), per)]
+        if max(batch_bytes(gl) for gl in groups) <= budget_bytes or per == 1:
+            return groups
+        n_batches *= 2
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -430,24 +451,7 @@ def run_ours(args):
     expanded = None
     if not args.no_expanded and rank == 0:
         ft = WT.expanded_forest(tree)
-        lens = list(ft.seg_len)
-        n_leaves = len(lens)
-
-        def batch_bytes(ls):
-            pb = TA.TreePlan([-1] * len(ls), ls)
-            nt = pb.n_tokens
-            ws = pb.workspace_size(hq, hkv, d)[1]
-            pb.close()
-            return nt * (4 * hq + 4 * hkv) * d * 2 + 4 * hq * nt + ws
-
-        free_b = torch.cuda.mem_get_info(dev)[0]
-        n_batches = 1
-        while True:
-            per = -(-n_leaves // n_batches)
-            groups = [lens[i:i + per] for i in range(0, n_leaves, per)]
-            if max(batch_bytes(gl) for gl in groups) <= 0.5 * free_b or per == 1:
-                break
-            n_batches *= 2
+        groups = chain_batches(TA, list(ft.seg_len), hq, hkv, d, 0.5 * torch.cuda.mem_get_info(dev)[0])
         eplans = [TA.TreePlan([-1] * len(gl), gl) for gl in groups]
         Ne = sum(pb.n_tokens for pb in eplans)
         Nmax = max(pb.n_tokens for pb in eplans)

@@ -50,3 +50,18 @@ def test_single_rank_needs_no_process_group():
     import bench
     assert bench.max_over_ranks(42.0, 1) == 42.0
     assert bench.job_throughput(2e12, 5, 1, 1000.0) == pytest.approx(10.0)
+
+
+def test_expanded_chain_batches():
+    """The expanded-trajectory leg splits its chains into equal contiguous
+    batches only when one batch would not fit the memory budget."""
+    import bench
+    import prefix_tree_attention_attn_gb300 as TA
+    lens = [5000, 7000, 3000, 9000, 4000, 6000, 8000, 2000]
+    whole = bench.chain_batches(TA, lens, 8, 2, 128, 1e15)
+    assert whole == [lens]
+    tight = bench.chain_batches(TA, lens, 8, 2, 128, 2e8)
+    assert len(tight) > 1 and [x for g in tight for x in g] == lens
+    assert len({len(g) for g in tight[:-1]}) == 1
+    one_each = bench.chain_batches(TA, lens, 8, 2, 128, 1.0)
+    assert one_each == [[x] for x in lens]

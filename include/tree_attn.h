@@ -120,6 +120,8 @@ typedef struct {
 
 /* Build a plan from a rollout tree or forest (host only, no GPU needed).
  * parent[v]: parent node id, -1 for a root.  seg_len[v] > 0: tokens of node v.
+ * n_nodes >= 1 (an empty tree is TREE_ATTN_ERR_INVALID_ARG; the smallest
+ * input is one node of one token).
  * Section: AReaL-DTA abstract (DFS traversal of the rollout prefix tree);
  * HARTS abstract (arbitrary rollout trees; prefix compression to compact
  * tokens).  opts may be NULL.  *out receives a new plan on success. */

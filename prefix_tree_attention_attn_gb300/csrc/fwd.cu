@@ -28,8 +28,8 @@
 // bf16) and feeds O += P V as the A operand, so it never touches shared
 // memory (whose bandwidth the MMAs' operand reads already use up).  The
 // softmax is bound by its FMA/ALU instructions, so pass 1 takes the maximum of
-// the raw logits (the scale is positive) and pass 2 is one FFMA into ex2 per
-// element.  O is rescaled in TMEM only when a
+// the raw logits (the scale is positive) and pass 2 is one packed FFMA per two
+// elements into ex2.  O is rescaled in TMEM only when a
 // row's running maximum grows by more than 2^8 (the accumulated sum and O keep
 // one common reference maximum, so the result is unchanged).
 //
@@ -293,7 +293,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NS, PER_SM>::NWARPS * 32, PER_SM)
                     tmem_st32(tS + cc * 32, v);
                 }
 #pragma unroll
-                for (int u = 0; u < 32; ++u) mraw = fmaxf(mraw, v[u]);
+                for (int u = 0; u < 32; u += 2) mraw = fmax3(mraw, v[u], v[u + 1]);
             }
             if (need_mask) tmem_wait_st();
             const float mx = mraw * sl2;   // softmax_scale > 0, so the maximum commutes with it
@@ -318,8 +318,12 @@ __global__ void __launch_bounds__(FwdCfg<D, NS, PER_SM>::NWARPS * 32, PER_SM)
             }
             const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
             // pass 2: P = 2^(s * scale*log2e - m) -> packed bf16 over S's first 64
-            // columns (each store lands on columns this thread has already read)
-            float lsum = 0.f;
+            // columns (each store lands on columns this thread has already read).
+            // The softmax warps are bound by instruction issue, so the argument and
+            // the row sum go through packed fp32 pairs (one instruction per two
+            // columns); the per-lane results equal the scalar fmaf / add.
+            const uint64_t scale2 = f32x2(sl2, sl2), negm2 = f32x2(-m_use, -m_use);
+            uint64_t lsum2 = f32x2(0.f, 0.f);
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 float v[32];
@@ -328,14 +332,17 @@ __global__ void __launch_bounds__(FwdCfg<D, NS, PER_SM>::NWARPS * 32, PER_SM)
                 uint32_t pw[16];
 #pragma unroll
                 for (int h = 0; h < 16; ++h) {
-                    const float a = fast_exp2(fmaf(v[2 * h], sl2, -m_use));
-                    const float b = fast_exp2(fmaf(v[2 * h + 1], sl2, -m_use));
-                    lsum += a + b;
+                    float ta, tb;
+                    f32x2_split(fma_f32x2(f32x2(v[2 * h], v[2 * h + 1]), scale2, negm2), ta, tb);
+                    const float a = fast_exp2(ta), b = fast_exp2(tb);
+                    lsum2 = add_f32x2(lsum2, f32x2(a, b));
                     pw[h] = pack_bf16x2(a, b);
                 }
                 tmem_st16(tS + cc * 16, pw);
             }
-            l_run += lsum;
+            float lsa, lsb;
+            f32x2_split(lsum2, lsa, lsb);
+            l_run += lsa + lsb;
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(b_pfull(s));

@@ -18,6 +18,15 @@ Two formulas, both fp64, on the expanded trajectories (one per leaf, first
 copy of each compact token kept; the copies agree):
 * ``forward_parallel`` -- the double sum above, as masked matrices;
 * ``forward_recurrent`` -- the state recursion token by token.
+
+``backward_parallel`` gives the gradients of a scalar loss whose gradient with
+respect to the compact O is dO, the same way the softmax oracle does: dO is
+split over the copies of each token (any split that sums to dO gives the same
+result, since every copy's output equals the compact one), and each
+trajectory's part is differentiated in closed form.  With A = Q K^T and the
+decay mask W, O = scale (A o W) V, so
+    dV = scale (A o W)^T dO,  dA = scale (dO V^T) o W,  dQ = dA K,  dK = dA^T Q,
+summed over the copies and, for dK and dV, over the q-heads of a kv-head.
 """
 from __future__ import annotations
 
@@ -69,3 +78,44 @@ def forward_recurrent(parent, seg_len, q, k, v, decay, scale):
                     if np.isnan(out[t, h, 0]):
                         out[t, h] = scale * (q[t, h] @ S)
     return out
+
+
+def backward_parallel(parent, seg_len, q, k, v, do, decay, scale, split="multiplicity"):
+    """dQ [N, hq, d], dK / dV [N, hkv, d] (fp64) for the compact gradient dO.
+
+    ``split`` = "multiplicity": copy weight 1 / (trajectories holding the
+    token); "first": all of a token's dO on its first trajectory (ascending
+    leaf id).
+    """
+    q, k, v, do = _as64(q), _as64(k), _as64(v), _as64(do)
+    gam = np.asarray(decay, dtype=np.float64)
+    N, hq, d = q.shape
+    hkv = k.shape[1]
+    G = hq // hkv
+    if split == "multiplicity":
+        w_tok = 1.0 / layout.multiplicity(parent, seg_len)
+    elif split != "first":
+        raise ValueError(split)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    seen = np.zeros(N, dtype=bool)
+    for _, idx in layout.trajectories(parent, seg_len):
+        L = len(idx)
+        if split == "multiplicity":
+            wt = w_tok[idx]
+        else:
+            wt = (~seen[idx]).astype(np.float64)
+            seen[idx] = True
+        diff = np.arange(L)[:, None] - np.arange(L)[None, :]
+        for h in range(hq):
+            g = h // G
+            W = np.where(diff >= 0, gam[g] ** np.maximum(diff, 0), 0.0)
+            Qt, Kt, Vt = q[idx, h], k[idx, g], v[idx, g]
+            dOt = do[idx, h] * wt[:, None]
+            M = (Qt @ Kt.T) * W
+            dA = scale * (dOt @ Vt.T) * W
+            np.add.at(dv[:, g], idx, scale * (M.T @ dOt))
+            np.add.at(dq[:, h], idx, dA @ Kt)
+            np.add.at(dk[:, g], idx, dA.T @ Qt)
+    return dq, dk, dv

@@ -60,3 +60,58 @@ def test_copies_agree_and_shared_prefix_equals_chain():
     c = WT.chain_tree([6])
     oc = OLN.forward_parallel(c.parent, c.seg_len, q[:6], k[:6], v[:6], [0.95], 1.0)
     assert np.abs(o[:6] - oc).max() < 1e-12
+
+
+# --------------------------------------------------------------------------
+# backward: pinned by finite differences of the forward oracle (O is linear in
+# each of Q, K and V, so central differences are exact up to rounding), the
+# closed form of one token, and the invariance of the dO split over copies
+# --------------------------------------------------------------------------
+
+def _loss(t, q, k, v, do, dec, scale):
+    return float((OLN.forward_parallel(t.parent, t.seg_len, q, k, v, dec, scale) * do).sum())
+
+
+@pytest.mark.parametrize("tree", [([-1, 0, 0], [2, 2, 1]), ([-1, 0, 1, 0, -1], [1, 2, 1, 2, 2])])
+def test_backward_equals_finite_differences(tree):
+    t = WT.Tree("fd", *tree)
+    N = t.n_tokens
+    q, k, v = rnd(N, 4, 2, 2, 11)
+    do = np.random.default_rng(12).normal(size=(N, 4, 2))
+    dec, scale, eps = [0.8, 1.0], 0.6, 1e-3
+    dq, dk, dv = OLN.backward_parallel(t.parent, t.seg_len, q, k, v, do, dec, scale)
+    for x, g in ((q, dq), (k, dk), (v, dv)):
+        fd = np.zeros_like(x)
+        for ix in np.ndindex(*x.shape):
+            keep = x[ix]
+            x[ix] = keep + eps
+            up = _loss(t, q, k, v, do, dec, scale)
+            x[ix] = keep - eps
+            dn = _loss(t, q, k, v, do, dec, scale)
+            x[ix] = keep
+            fd[ix] = (up - dn) / (2 * eps)
+        assert np.abs(g - fd).max() <= 1e-8 * max(1.0, np.abs(fd).max())
+
+
+def test_backward_one_token_closed_form():
+    t = WT.chain_tree([1])
+    q, k, v = rnd(1, 1, 1, 3, 5)
+    do = np.random.default_rng(6).normal(size=(1, 1, 3))
+    s = 0.9
+    dq, dk, dv = OLN.backward_parallel(t.parent, t.seg_len, q, k, v, do, [0.5], s)
+    qk, dov = float(q[0, 0] @ k[0, 0]), float(do[0, 0] @ v[0, 0])
+    assert np.abs(dq[0, 0] - s * dov * k[0, 0]).max() < 1e-14
+    assert np.abs(dk[0, 0] - s * dov * q[0, 0]).max() < 1e-14
+    assert np.abs(dv[0, 0] - s * qk * do[0, 0]).max() < 1e-14
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_backward_split_invariance(seed):
+    rng = np.random.default_rng(40 + seed)
+    t = WT.random_tree(rng, int(rng.integers(3, 8)), [1, 2, 5], n_roots=1 + seed % 2)
+    q, k, v = rnd(t.n_tokens, 2, 1, 3, seed)
+    do = rng.normal(size=(t.n_tokens, 2, 3))
+    a = OLN.backward_parallel(t.parent, t.seg_len, q, k, v, do, [0.9], 1.0, split="multiplicity")
+    b = OLN.backward_parallel(t.parent, t.seg_len, q, k, v, do, [0.9], 1.0, split="first")
+    for x, y in zip(a, b):
+        assert np.abs(x - y).max() < 1e-11

@@ -3,7 +3,7 @@
 //
 // One CTA = one 128-row q-tile x NS q-heads of the same kv-head group.  The CTA
 // visits only the kv-tiles in the q-tile's ancestor interval list; empty tiles
-// are never loaded.  Two shapes:
+// are never loaded.  Three shapes, chosen per plan and head layout:
 //  * NS = 2 (even group size, long kv-tile lists): the two q-heads read the same
 //    key tiles, so every K/V tile is loaded once for both; one CTA per SM with a
 //    deep K/V ring.
@@ -25,11 +25,11 @@
 // Pipeline on the tensor core:  S0(0) S1(0) | PV0(0) S0(1) | PV1(0) S1(1) | ...
 // While softmax group 0 turns S0(j) into P0(j), the tensor core runs q-head 1's
 // MMAs, and the other way round.  P is written back over S in TMEM (packed
-// bf16) and feeds O += P V as the A operand, so it never touches shared
-// memory (whose bandwidth the MMAs' operand reads already use up).  The
-// softmax is bound by its FMA/ALU instructions, so pass 1 takes the maximum of
-// the raw logits (the scale is positive) and pass 2 is one packed FFMA per two
-// elements into ex2.  O is rescaled in TMEM only when a
+// bf16) and feeds O += P V as the A operand, so it never goes through shared
+// memory.  The softmax warps, not the MMAs, set the pace (their instruction
+// issue), so pass 1 takes the maximum of the raw logits (the scale is
+// positive) three at a time and pass 2 is one packed FFMA per two elements
+// into ex2.  O is rescaled in TMEM only when a
 // row's running maximum grows by more than 2^8 (the accumulated sum and O keep
 // one common reference maximum, so the result is unchanged).
 //

@@ -19,6 +19,14 @@ copy of each compact token kept; the copies agree):
 * ``forward_parallel`` -- the double sum above, as masked matrices;
 * ``forward_recurrent`` -- the state recursion token by token.
 
+``backward_recurrent`` is a second, independent formula on the compact tokens:
+with S_t the state after token t (S_t = gamma S_prev(t) + k_t v_t^T, prev(t)
+the token before t on its path), O_t = scale q_t^T S_t, and the adjoint
+R_t = dL/dS_t = scale sum_h q_t^h dO_t^h^T + gamma sum_{u: prev(u) = t} R_u
+(summed over every continuation of t: the next token of its node, or the first
+token of each child node), so dQ_t = scale S_t dO_t, dK_t = R_t v_t and
+dV_t = R_t^T k_t.
+
 ``backward_parallel`` gives the gradients of a scalar loss whose gradient with
 respect to the compact O is dO, the same way the softmax oracle does: dO is
 split over the copies of each token (any split that sums to dO gives the same
@@ -118,4 +126,42 @@ def backward_parallel(parent, seg_len, q, k, v, do, decay, scale, split="multipl
             np.add.at(dv[:, g], idx, scale * (M.T @ dOt))
             np.add.at(dq[:, h], idx, dA @ Kt)
             np.add.at(dk[:, g], idx, dA.T @ Qt)
+    return dq, dk, dv
+
+
+def backward_recurrent(parent, seg_len, q, k, v, do, decay, scale):
+    """The same gradients from the state and adjoint recursions over the
+    compact tokens (no trajectory expansion): states forward in packed order,
+    adjoints backward, each token's adjoint summing over its continuations."""
+    q, k, v, do = _as64(q), _as64(k), _as64(v), _as64(do)
+    gam = np.asarray(decay, dtype=np.float64)
+    N, hq, d = q.shape
+    hkv = k.shape[1]
+    G = hq // hkv
+    order, off, _ = layout.packed_layout(parent, seg_len)
+    prev = np.full(N, -1, dtype=np.int64)       # token before t on its path
+    for u in order:
+        for m in range(seg_len[u]):
+            t = off[u] + m
+            if m > 0:
+                prev[t] = t - 1
+            elif parent[u] >= 0:
+                prev[t] = off[parent[u]] + seg_len[parent[u]] - 1
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for g in range(hkv):
+        S = np.zeros((N, d, d))
+        for t in range(N):                      # parents come before children in packed order
+            base = gam[g] * S[prev[t]] if prev[t] >= 0 else 0.0
+            S[t] = base + np.outer(k[t, g], v[t, g])
+        R = np.zeros((N, d, d))
+        for t in range(N - 1, -1, -1):          # every continuation of t comes after t
+            for h in range(g * G, (g + 1) * G):
+                R[t] += scale * np.outer(q[t, h], do[t, h])
+                dq[t, h] = scale * (S[t] @ do[t, h])
+            if prev[t] >= 0:
+                R[prev[t]] += gam[g] * R[t]
+            dk[t, g] = R[t] @ v[t, g]
+            dv[t, g] = R[t].T @ k[t, g]
     return dq, dk, dv

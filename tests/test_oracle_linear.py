@@ -115,3 +115,18 @@ def test_backward_split_invariance(seed):
     b = OLN.backward_parallel(t.parent, t.seg_len, q, k, v, do, [0.9], 1.0, split="first")
     for x, y in zip(a, b):
         assert np.abs(x - y).max() < 1e-11
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_backward_recurrent_equals_parallel(seed):
+    """The adjoint recursion over compact tokens (no expansion) against the
+    per-trajectory VJP with the dO split over copies."""
+    rng = np.random.default_rng(60 + seed)
+    t = WT.random_tree(rng, int(rng.integers(2, 9)), [1, 2, 3, 6], n_roots=1 + seed % 2)
+    q, k, v = rnd(t.n_tokens, 4, 2, 3, seed)
+    do = rng.normal(size=(t.n_tokens, 4, 3))
+    dec = [0.85, 1.0]
+    a = OLN.backward_parallel(t.parent, t.seg_len, q, k, v, do, dec, 0.7)
+    b = OLN.backward_recurrent(t.parent, t.seg_len, q, k, v, do, dec, 0.7)
+    for x, y in zip(a, b):
+        assert np.abs(x - y).max() <= 1e-10 * max(1.0, np.abs(x).max())

@@ -52,6 +52,29 @@ int tree_attn_linear_fwd(tree_attn_plan_t plan, const void* q, const void* k, co
                          const float* decay, int32_t hq, int32_t hkv, int32_t d, float scale,
                          void* workspace, size_t ws_bytes, void* stream);
 
+/* Backward of tree_attn_linear_fwd for the compact output gradient dout
+ * ([N, hq, d] bf16, the gradient of one scalar loss; per-trajectory weights
+ * are folded into it by the caller):
+ *
+ *   dQ_i = scale sum_{j on i's path, j <= i} gamma^(pos_i - pos_j) (dO_i . v_j) k_j
+ *   dK_j = scale sum_h sum_{i: j on i's path, i >= j} gamma^(pos_i - pos_j) (dO_i^h . v_j) q_i^h
+ *   dV_j = scale sum_h sum_{i: j on i's path, i >= j} gamma^(pos_i - pos_j) (q_i^h . k_j) dO_i^h
+ *
+ * (h over the q-heads of j's kv-head).  dQ is the forward with (q, k, v) =
+ * (dO, V, K).  For dK and dV the adjoint of the state runs the other way from
+ * the forward's handoff: per chunk F = scale sum_h Q_h^T diag(gamma^(m+1))
+ * dO_h, then in reverse packed order Rsum(chunk) = the sum of the entering
+ * adjoints of the chunks that continue it (the next chunk of its node, or the
+ * first chunk of every child node), R_in = F + gamma^L Rsum, and per chunk
+ * dK = diag(gamma^(L-1-m)) V Rsum^T + sum_h dA_h^T Q_h,
+ * dV = diag(gamma^(L-1-m)) K Rsum + sum_h P_h^T dO_h (tensor cores, the decay
+ * masks in registers).  Outputs dq [N, hq, d], dk / dv [N, hkv, d] bf16,
+ * written (not accumulated).  Same workspace as the forward (contents on entry
+ * ignored), same argument rules.  Asynchronous on `stream`. */
+int tree_attn_linear_bwd(tree_attn_plan_t plan, const void* q, const void* k, const void* v, const void* dout,
+                         void* dq, void* dk, void* dv, const float* decay, int32_t hq, int32_t hkv, int32_t d,
+                         float scale, void* workspace, size_t ws_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

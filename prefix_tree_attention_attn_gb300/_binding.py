@@ -69,6 +69,9 @@ SIGNATURES = {
     "tree_attn_linear_fwd": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                        C.c_int32, C.c_int32, C.c_int32, C.c_float, C.c_void_p, C.c_size_t,
                                        C.c_void_p]),
+    "tree_attn_linear_bwd": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                       C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_int32,
+                                       C.c_float, C.c_void_p, C.c_size_t, C.c_void_p]),
     # include/tree_loss.h
     "tree_attn_plan_trajectory_info": (C.c_int, [C.c_void_p, c_int32_p, c_int64_p]),
     "tree_attn_plan_trajectories": (C.c_int, [C.c_void_p, c_int32_p, c_int64_p, c_int32_p]),

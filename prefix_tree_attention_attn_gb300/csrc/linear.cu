@@ -2,7 +2,7 @@
 // recurrent state handed from every node to its children
 // (include/tree_linear.h).
 //
-// Three kernels per call:
+// Forward, three kernels per call:
 //   lin_delta_kernel  per (chunk, kv-head): dS = K^T diag(gamma^(L-1-m)) V on
 //                     the tensor core (M = 128 key features, N = 128 value
 //                     features, K = the chunk's tokens), read out of TMEM to
@@ -450,6 +450,379 @@ LinWs lin_layout(const tree_attn_plan_s* P, int32_t hkv) {
     return w;
 }
 
+// ============================== backward ======================================
+// dQ is itself a tree linear attention: scale * sum over the path of
+// gamma^(distance) (dO_i . v_j) k_j -- the three forward kernels with
+// (q, k, v) = (dO, V, K).  dK and dV need the adjoint of the state, which flows
+// the other way, from every node into its parent (summed over the children):
+//   F_c      = scale sum_h Q_h^T diag(gamma^(m+1)) dO_h      (lin_bwd_f_kernel)
+//   Rsum(c)  = sum over the chunks c' that continue c of R_in(c'),
+//   R_in(c)  = F_c + gamma^L Rsum(c)                          (lin_bwd_scan_kernel)
+//   dK rows  = gamma^(L-1-m') Rsum v_m'  + sum_h (dA_h^T Q_h)
+//   dV rows  = gamma^(L-1-m') Rsum^T k_m' + sum_h (P_h^T dO_h) (lin_bwd_kv_kernel)
+// with P_h^T[m', m] = scale (k_m' . q_m) gamma^(m-m') and dA_h^T[m', m] =
+// scale (v_m' . dO_m) gamma^(m-m') for m' <= m < L.
+
+// ---- F per (chunk, kv-head), the group's q-heads accumulated in TMEM ----------
+// warps 0-3: lane r = token row r (scaling dO) and key feature r (read-out);
+// warp 4: TMEM owner, lane 0 loads and issues.
+constexpr int kAdjSmem = 1024 + 2 * kTile;
+
+__global__ void __launch_bounds__(160, 1)
+    lin_bwd_f_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                     const int32_t* __restrict__ chunks, const float* __restrict__ decay, int hq, int hkv,
+                     float scale, float* __restrict__ f_out, int* status) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const uint32_t sb = smem_u32(smem);
+    const int warp = threadIdx.x >> 5;
+    if (sb & 1023u) {
+        if (threadIdx.x == 0) report_status(status, -5);
+        return;
+    }
+    const int G = hq / hkv;
+    const int chunk = blockIdx.x / hkv, g = blockIdx.x % hkv;
+    const int off = chunks[4 * chunk], L = chunks[4 * chunk + 1];
+    const uint32_t b_full = sb, b_scaled = sb + 8, b_mma = sb + 16, holder = sb + 24;
+    const uint32_t qa = sb + 1024, da = qa + kTile;
+    if (threadIdx.x == 0) {
+        mbar_init(b_full, 1);
+        mbar_init(b_scaled, 128);
+        mbar_init(b_mma, 1);
+        fence_mbar_init();
+    }
+    if (warp == 4) tmem_alloc(holder, 128);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + 24);
+    const float lg = log2f(decay[g]);
+    bool ok = true;
+    for (int n = 0; n < G; ++n) {
+        if (threadIdx.x == 128 && ok) {
+            // Q and dO of the previous head must have been read by its MMAs
+            if (n > 0) ok = mbar_wait(b_mma, (n - 1) & 1, status, 94);
+            if (ok) {
+                mbar_expect_tx(b_full, 2 * kTile);
+                for (int blk = 0; blk < 2; ++blk) {
+                    tma_load_3d(qa + blk * 16384, &tm_q, blk * 64, g * G + n, off, b_full);
+                    tma_load_3d(da + blk * 16384, &tm_do, blk * 64, g * G + n, off, b_full);
+                }
+            }
+        }
+        if (warp < 4) {
+            if (ok) ok = mbar_wait(b_full, n & 1, status, 95);
+            if (ok) {
+                // dO row r times scale * gamma^(r+1) (0 past the chunk), in place
+                const int r = threadIdx.x;
+                const float w = r < L ? scale * exp2f((float)(r + 1) * lg) : 0.f;
+#pragma unroll
+                for (int blk = 0; blk < 2; ++blk) {
+                    uint4* row = reinterpret_cast<uint4*>(smem + 1024 + kTile + blk * 16384 + r * 128);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        uint4 x = row[c];
+                        uint32_t* u = reinterpret_cast<uint32_t*>(&x);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            u[e] = pack_bf16x2(__uint_as_float(u[e] << 16) * w,
+                                               __uint_as_float(u[e] & 0xffff0000u) * w);
+                        row[c] = x;
+                    }
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(b_scaled);
+            }
+        }
+        if (threadIdx.x == 128 && ok) {
+            ok = mbar_wait(b_scaled, n & 1, status, 96);
+            if (ok) {
+                tc_fence_after();
+                constexpr uint32_t ID = idesc_bf16(128, 128, true, true);   // Q^T (MN-major) x dO_w (MN-major)
+#pragma unroll
+                for (int k = 0; k < kChunk / 16; ++k)
+                    mma_bf16_ss(tmem, sdesc_sw128(qa + k * 2048, 16384, 1024),
+                                sdesc_sw128(da + k * 2048, 16384, 1024), ID, (n > 0 || k > 0) ? 1u : 0u);
+                mma_commit(b_mma);
+            }
+        }
+    }
+    if (warp < 4) {
+        if (ok) ok = mbar_wait(b_mma, (G - 1) & 1, status, 97);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+            tc_fence_after();
+            const int r = threadIdx.x;   // key feature
+            const uint32_t lane_base = tmem + ((uint32_t)(warp << 5) << 16);
+            float4* dst = reinterpret_cast<float4*>(f_out + (((size_t)chunk * hkv + g) * kD + r) * kD);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                float v[32];
+                tmem_ld32(lane_base + cc * 32, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    dst[cc * 8 + u] = make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 4) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 128);
+    }
+}
+
+// ---- adjoints, node by node in reverse packed order --------------------------
+// One thread per (state entry, kv-head).  A node's children come after it in
+// packed order, so walking backwards every child's entering adjoint has been
+// added into its parent's slot (csum) before the parent is reached.
+__global__ void __launch_bounds__(256) lin_bwd_scan_kernel(const int32_t* __restrict__ lnodes, int n_nodes,
+                                                         const int32_t* __restrict__ chunks,
+                                                         const float* __restrict__ decay, int hkv,
+                                                         const float* __restrict__ f_in, float* __restrict__ rsum,
+                                                         float* __restrict__ csum) {
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    const int g = blockIdx.y;
+    const size_t dd = (size_t)kD * kD;
+    const float lg = log2f(decay[g]);
+    for (int k = 0; k < n_nodes; ++k) csum[((size_t)k * hkv + g) * dd + e] = 0.f;
+    for (int k = n_nodes - 1; k >= 0; --k) {
+        const int par = lnodes[4 * k], c0 = lnodes[4 * k + 1], nc = lnodes[4 * k + 2];
+        float acc = csum[((size_t)k * hkv + g) * dd + e];   // sum over the children's entering adjoints
+        for (int c = c0 + nc - 1; c >= c0; --c) {
+            const size_t at = ((size_t)c * hkv + g) * dd + e;
+            rsum[at] = acc;
+            acc = f_in[at] + exp2f((float)chunks[4 * c + 1] * lg) * acc;
+        }
+        if (par >= 0) csum[((size_t)par * hkv + g) * dd + e] += acc;
+    }
+}
+
+// ---- dK, dV per (chunk, kv-head) ------------------------------------------------
+// TMEM: dK [0, 128), dV [128, 256), S^T -> P^T [256, 384), A^T -> dA^T [384, 512).
+// warps 0-3: lane m' = key row m' (and key feature when staging Rsum); warp 4:
+// loads; warp 5: TMEM owner, lane 0 issues the MMAs.  The group's q-heads run
+// one after another through one Q / dO slot pair.
+constexpr int kKvSmem = 1024 + 5 * kTile;   // K, V, Rsum (bf16), Q, dO
+
+__global__ void __launch_bounds__(192, 1)
+    lin_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                      const int32_t* __restrict__ chunks, const float* __restrict__ decay,
+                      const float* __restrict__ rsum, uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, int hq,
+                      int hkv, float scale, int* status) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const uint32_t sb = smem_u32(smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (sb & 1023u) {
+        if (threadIdx.x == 0) report_status(status, -5);
+        return;
+    }
+    const int G = hq / hkv;
+    const int chunk = blockIdx.x / hkv, g = blockIdx.x % hkv;
+    const int off = chunks[4 * chunk], L = chunks[4 * chunk + 1];
+    auto bar = [&](int i) { return sb + 8u * (uint32_t)i; };
+    const uint32_t b_kv = bar(0), b_r = bar(1), b_inter = bar(2), b_scaled = bar(3), b_qf = bar(4), b_sa = bar(5),
+                   b_pa = bar(6), b_qe = bar(7), b_done = bar(8), b_drain = bar(9), holder = bar(10);
+    const uint32_t ka = sb + 1024, va = ka + kTile, ra = va + kTile, qa = ra + kTile, da = qa + kTile;
+    if (threadIdx.x == 0) {
+        mbar_init(b_kv, 1);
+        mbar_init(b_r, 128);
+        mbar_init(b_inter, 1);
+        mbar_init(b_scaled, 128);
+        mbar_init(b_qf, 1);
+        mbar_init(b_sa, 1);
+        mbar_init(b_pa, 128);
+        mbar_init(b_qe, 1);
+        mbar_init(b_done, 1);
+        mbar_init(b_drain, 1);
+        fence_mbar_init();
+    }
+    if (warp == 5) tmem_alloc(holder, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + 8 * 10);
+
+    if (warp == 4) {
+        if (lane == 0) {
+            mbar_expect_tx(b_kv, 2 * kTile);
+            for (int blk = 0; blk < 2; ++blk) {
+                tma_load_3d(ka + blk * 16384, &tm_k, blk * 64, g, off, b_kv);
+                tma_load_3d(va + blk * 16384, &tm_v, blk * 64, g, off, b_kv);
+            }
+            bool ok = true;
+            for (int n = 0; n < G && ok; ++n) {
+                if (n > 0) ok = mbar_wait(b_qe, (n - 1) & 1, status, 100);
+                if (!ok) break;
+                mbar_expect_tx(b_qf, 2 * kTile);
+                for (int blk = 0; blk < 2; ++blk) {
+                    tma_load_3d(qa + blk * 16384, &tm_q, blk * 64, g * G + n, off, b_qf);
+                    tma_load_3d(da + blk * 16384, &tm_do, blk * 64, g * G + n, off, b_qf);
+                }
+            }
+        }
+    } else if (warp == 5) {
+        if (lane == 0) {
+            constexpr uint32_t ID_KK = idesc_bf16(128, 128, false, false);   // B K-major
+            constexpr uint32_t ID_KM = idesc_bf16(128, 128, false, true);    // B MN-major
+            bool ok = mbar_wait(b_kv, 0, status, 101);
+            if (ok) ok = mbar_wait(b_r, 0, status, 102);
+            if (ok) {
+                tc_fence_after();
+                // carried-in parts: dK = V Rsum^T (Rsum rows = key features, i.e. K-major
+                // for this product), dV = K Rsum (the same tile read MN-major)
+#pragma unroll
+                for (int k = 0; k < kD / 16; ++k) {
+                    const uint32_t o = (k >> 2) * 16384 + (k & 3) * 32;
+                    mma_bf16_ss(tmem, sdesc_sw128(va + o, 16, 1024), sdesc_sw128(ra + o, 16, 1024), ID_KK, k > 0);
+                }
+#pragma unroll
+                for (int k = 0; k < kD / 16; ++k) {
+                    const uint32_t o = (k >> 2) * 16384 + (k & 3) * 32;
+                    mma_bf16_ss(tmem + 128, sdesc_sw128(ka + o, 16, 1024), sdesc_sw128(ra + k * 2048, 16384, 1024),
+                                ID_KM, k > 0);
+                }
+                mma_commit(b_inter);
+            }
+            for (int n = 0; n < G && ok; ++n) {
+                ok = mbar_wait(b_qf, n & 1, status, 103);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < kD / 16; ++k) {   // S^T = K Q^T
+                    const uint32_t o = (k >> 2) * 16384 + (k & 3) * 32;
+                    mma_bf16_ss(tmem + 256, sdesc_sw128(ka + o, 16, 1024), sdesc_sw128(qa + o, 16, 1024), ID_KK,
+                                k > 0);
+                }
+#pragma unroll
+                for (int k = 0; k < kD / 16; ++k) {   // A^T = V dO^T
+                    const uint32_t o = (k >> 2) * 16384 + (k & 3) * 32;
+                    mma_bf16_ss(tmem + 384, sdesc_sw128(va + o, 16, 1024), sdesc_sw128(da + o, 16, 1024), ID_KK,
+                                k > 0);
+                }
+                mma_commit(b_sa);
+                ok = mbar_wait(b_pa, n & 1, status, 104);
+                if (ok && n == 0) ok = mbar_wait(b_scaled, 0, status, 105);   // carried-in rows scaled
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < kChunk / 16; ++k)   // dV += P^T dO
+                    mma_bf16_ts(tmem + 128, tmem + 256 + k * 8, sdesc_sw128(da + k * 2048, 16384, 1024), ID_KM, 1u);
+#pragma unroll
+                for (int k = 0; k < kChunk / 16; ++k)   // dK += dA^T Q
+                    mma_bf16_ts(tmem, tmem + 384 + k * 8, sdesc_sw128(qa + k * 2048, 16384, 1024), ID_KM, 1u);
+                mma_commit(b_qe);   // Q / dO slots and T1 / T2 free again
+            }
+            if (ok) mma_commit(b_done);
+            mma_commit(b_drain);
+            mbar_wait(b_drain, 0, status, 106);
+        }
+        __syncwarp();
+    } else {
+        const int m = threadIdx.x;   // key row m'; key feature when staging Rsum
+        const uint32_t lane_base = tmem + ((uint32_t)(warp << 5) << 16);
+        const float lg = log2f(decay[g]);
+        // Rsum (fp32 [key feature][value feature]) -> bf16, laid out like a value tile
+        {
+            const float4* src = reinterpret_cast<const float4*>(rsum + (((size_t)chunk * hkv + g) * kD + m) * kD);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float4 a4 = src[2 * j], b4 = src[2 * j + 1];
+                const int blk = j >> 3, cj = j & 7;
+                st_shared_v4(ra + blk * 16384 + sw128_offset(m, cj), pack_bf16x2(a4.x, a4.y),
+                             pack_bf16x2(a4.z, a4.w), pack_bf16x2(b4.x, b4.y), pack_bf16x2(b4.z, b4.w));
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(b_r);
+        }
+        bool ok = mbar_wait(b_inter, 0, status, 107);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+            // carried-in rows weigh gamma^(L-1-m') (0 past the chunk)
+            tc_fence_after();
+            const float w = m < L ? exp2f((float)(L - 1 - m) * lg) : 0.f;
+#pragma unroll
+            for (int part = 0; part < 2; ++part)
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    float v[32];
+                    tmem_ld32(lane_base + part * 128 + cc * 32, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) v[u] *= w;
+                    tmem_st32(lane_base + part * 128 + cc * 32, v);
+                }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(b_scaled);
+        }
+        for (int n = 0; n < G; ++n) {
+            if (ok) ok = mbar_wait(b_sa, n & 1, status, 108);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) continue;
+            tc_fence_after();
+            // P^T[m', m] = scale S^T gamma^(m-m'), dA^T[m', m] = scale A^T gamma^(m-m'),
+            // for m' <= m < L; packed bf16 over the first 64 columns of each region
+#pragma unroll 2
+            for (int cc = 0; cc < 8; ++cc) {   // 16 columns at a time
+                float s[16], a[16];
+                tmem_ld16(lane_base + 256 + cc * 16, s);
+                tmem_ld16(lane_base + 384 + cc * 16, a);
+                tmem_wait_ld();
+                uint32_t pw[8], aw[8];
+#pragma unroll
+                for (int w2 = 0; w2 < 8; ++w2) {
+                    const int c0 = cc * 16 + 2 * w2, c1 = c0 + 1;
+                    const float w0 = (m <= c0 && c0 < L) ? scale * exp2f((float)(c0 - m) * lg) : 0.f;
+                    const float w1 = (m <= c1 && c1 < L) ? scale * exp2f((float)(c1 - m) * lg) : 0.f;
+                    pw[w2] = pack_bf16x2(s[2 * w2] * w0, s[2 * w2 + 1] * w1);
+                    aw[w2] = pack_bf16x2(a[2 * w2] * w0, a[2 * w2 + 1] * w1);
+                }
+                // over columns this thread has already read
+                tmem_st8(lane_base + 256 + cc * 8, pw);
+                tmem_st8(lane_base + 384 + cc * 8, aw);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(b_pa);
+        }
+        if (ok) ok = mbar_wait(b_done, 0, status, 109);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+            tc_fence_after();
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+                uint4* dst = reinterpret_cast<uint4*>((part ? dv : dk) + ((size_t)(off + m) * hkv + g) * kD);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    float v[32];
+                    tmem_ld32(lane_base + part * 128 + cc * 32, v);
+                    tmem_wait_ld();
+                    if (m < L) {
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            uint4 x;
+                            x.x = pack_bf16x2(v[8 * w], v[8 * w + 1]);
+                            x.y = pack_bf16x2(v[8 * w + 2], v[8 * w + 3]);
+                            x.z = pack_bf16x2(v[8 * w + 4], v[8 * w + 5]);
+                            x.w = pack_bf16x2(v[8 * w + 6], v[8 * w + 7]);
+                            dst[cc * 4 + w] = x;
+                        }
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 }  // namespace
@@ -512,6 +885,62 @@ int tree_attn_linear_fwd(tree_attn_plan_t P, const void* q, const void* k, const
     if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
     lin_out_kernel<<<(unsigned)(nc * hkv), 192, kOutSmem, s>>>(tq, tk, tv, D->chunks, decay, s_in,
                                                               static_cast<uint16_t*>(o), hq, hkv, scale, status);
+    return cudaGetLastError() == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
+}
+
+
+int tree_attn_linear_bwd(tree_attn_plan_t P, const void* q, const void* k, const void* v, const void* dout,
+                         void* dq, void* dk, void* dv, const float* decay, int32_t hq, int32_t hkv, int32_t d,
+                         float scale, void* workspace, size_t ws_bytes, void* stream) {
+    if (!P || !q || !k || !v || !dout || !dq || !dk || !dv || !decay || hq <= 0 || hkv <= 0 || hq % hkv != 0)
+        return TREE_ATTN_ERR_INVALID_ARG;
+    if (d != kD || P->block != kChunk) return TREE_ATTN_ERR_UNSUPPORTED;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return TREE_ATTN_ERR_INVALID_ARG;
+    for (const void* p : {q, k, v, dout, (const void*)dq, (const void*)dk, (const void*)dv})
+        if (!aligned(p, 16)) return TREE_ATTN_ERR_ALIGNMENT;
+    if (!aligned(decay, 4) || !aligned(workspace, 256)) return TREE_ATTN_ERR_ALIGNMENT;
+    DevicePlan* D = nullptr;
+    int st = ensure_lin_device(P, &D);
+    if (st) return st;
+    const LinWs w = lin_layout(P, hkv);
+    if (!workspace || ws_bytes < w.total) return TREE_ATTN_ERR_WORKSPACE;
+    const int64_t nc = (int64_t)(P->lin.chunks.size() / 4);
+    if (nc * hq > INT32_MAX || nc * hkv > INT32_MAX) return TREE_ATTN_ERR_TOO_LARGE;
+    CUtensorMap tq, tk, tv, tdo;
+    if ((st = make_tensor_map(&tq, q, P->N, hq, d)) || (st = make_tensor_map(&tk, k, P->N, hkv, d)) ||
+        (st = make_tensor_map(&tv, v, P->N, hkv, d)) || (st = make_tensor_map(&tdo, dout, P->N, hq, d)))
+        return st;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int* status = nullptr;
+    if ((st = get_status_ptr(dev, &status))) return st;
+    char* ws = static_cast<char*>(workspace);
+    float* r0 = reinterpret_cast<float*>(ws + w.ds);      // dS', then F
+    float* r1 = reinterpret_cast<float*>(ws + w.s_in);    // S'_in, then Rsum
+    float* r2 = reinterpret_cast<float*>(ws + w.s_out);   // S'_out, then the per-node child sums
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaFuncSetAttribute(lin_delta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDeltaSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(lin_out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kOutSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(lin_bwd_f_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAdjSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(lin_bwd_kv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kKvSmem) != cudaSuccess)
+        return TREE_ATTN_ERR_CUDA;
+    // dQ: the forward with (q, k, v) = (dO, V, K)
+    lin_delta_kernel<<<(unsigned)(nc * hkv), 160, kDeltaSmem, s>>>(tv, tk, D->chunks, decay, hkv, r0, status);
+    if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
+    lin_scan_kernel<<<dim3(kD * kD / 256, hkv), 256, 0, s>>>(D->lnodes, P->n_nodes, D->chunks, decay, hkv, r0, r1, r2);
+    if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
+    lin_out_kernel<<<(unsigned)(nc * hkv), 192, kOutSmem, s>>>(tdo, tv, tk, D->chunks, decay, r1,
+                                                              static_cast<uint16_t*>(dq), hq, hkv, scale, status);
+    if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
+    // dK, dV: adjoint increments, the reverse scan, then the per-chunk products
+    lin_bwd_f_kernel<<<(unsigned)(nc * hkv), 160, kAdjSmem, s>>>(tq, tdo, D->chunks, decay, hq, hkv, scale, r0, status);
+    if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
+    lin_bwd_scan_kernel<<<dim3(kD * kD / 256, hkv), 256, 0, s>>>(D->lnodes, P->n_nodes, D->chunks, decay, hkv, r0, r1,
+                                                                 r2);
+    if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
+    lin_bwd_kv_kernel<<<(unsigned)(nc * hkv), 192, kKvSmem, s>>>(tq, tk, tv, tdo, D->chunks, decay, r1,
+                                                                 static_cast<uint16_t*>(dk), static_cast<uint16_t*>(dv),
+                                                                 hq, hkv, scale, status);
     return cudaGetLastError() == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
 }
 

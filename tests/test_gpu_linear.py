@@ -8,7 +8,7 @@ import torch
 
 from oracle import linear as OLN
 from prefix_tree_attention_attn_gb300 import TreePlan, device_status
-from prefix_tree_attention_attn_gb300.linear import linear_workspace, tree_linear_fwd
+from prefix_tree_attention_attn_gb300.linear import linear_workspace, tree_linear_bwd, tree_linear_fwd
 from workloads import tensors as WX
 from workloads import trees as WT
 
@@ -66,3 +66,65 @@ def test_segment_tree_workload():
     plan = check(t, 4, 1, [0.999], 5)
     nc, ws = linear_workspace(plan, 1, 128)
     assert nc == sum((L + 127) // 128 for L in t.seg_len)
+
+
+# --------------------------------------------------------------------------
+# backward: dQ (the forward with (dO, V, K)), dK and dV (the reverse adjoint
+# scan) against the fp64 oracle's per-trajectory VJP
+# --------------------------------------------------------------------------
+
+def check_bwd(t, hq, hkv, decay, seed):
+    x = WX.draw_inputs(t.n_tokens, WX.HeadConfig(hq, hkv, 128), WX.ValueRecipe(1, 1, 1, 1, 1), seed)
+    plan = TreePlan(t.parent, t.seg_len)
+    dec = torch.tensor(decay, dtype=torch.float32)
+    scale = 1 / np.sqrt(128)
+    dq, dk, dv = tree_linear_bwd(plan, x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), x["do"].cuda(), dec.cuda(),
+                                 scale)
+    torch.cuda.synchronize()
+    want = OLN.backward_parallel(t.parent, t.seg_len, x["q"], x["k"], x["v"], x["do"], decay, scale)
+    for name, g, w in zip(("dq", "dk", "dv"), (dq, dk, dv), want):
+        got = g.float().cpu().numpy()
+        for h in range(got.shape[1]):
+            e = rel(got[:, h], w[:, h])
+            assert e <= REL, (name, h, e)
+
+
+@pytest.mark.parametrize("parent,seg_len,hq,hkv,decay", [
+    ([-1], [1], 2, 1, [1.0]),
+    ([-1], [300], 2, 2, [1.0, 0.98]),
+    ([-1, 0, 0], [127, 129, 1], 4, 2, [0.95, 1.0]),
+    ([-1, 0, 0, 1, 1, 2], [128, 200, 5, 64, 300, 33], 4, 1, [0.99]),
+    ([-1, 0, 1, -1, 3], [70, 60, 5, 300, 2], 3, 3, [1.0, 0.9, 0.995]),
+])
+def test_bwd_small_trees(parent, seg_len, hq, hkv, decay):
+    check_bwd(WT.Tree("s", parent, seg_len), hq, hkv, decay, 21)
+
+
+@pytest.mark.parametrize("seed", range(2))
+def test_bwd_random_trees(seed):
+    rng = np.random.default_rng(400 + seed)
+    t = WT.random_tree(rng, int(rng.integers(3, 10)), [1, 17, 127, 128, 129, 255], n_roots=1 + seed % 2)
+    check_bwd(t, 4, 2, [0.97, 1.0], 40 + seed)
+
+
+def test_bwd_timing_segment_tree():
+    """Times one backward on the segment tree (32 q-heads, 8 kv-heads) and
+    checks the outputs are finite; the parity cases above pin the values."""
+    t = WT.load_tree("segment_tree")
+    x = WX.draw_inputs(t.n_tokens, WX.HeadConfig(32, 8, 128), WX.ValueRecipe(1, 1, 1, 1, 1), 9, device="cuda")
+    plan = TreePlan(t.parent, t.seg_len)
+    dec = torch.full((8,), 0.999, dtype=torch.float32, device="cuda")
+    _, need = linear_workspace(plan, 8, 128)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    args = (plan, x["q"], x["k"], x["v"], x["do"], dec, 1 / np.sqrt(128))
+    for _ in range(3):
+        out = tree_linear_bwd(*args, workspace=ws)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(10):
+        out = tree_linear_bwd(*args, workspace=ws)
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / 10
+    print(f"\nlinear bwd segment tree: {ms:.3f} ms, {t.n_tokens / ms / 1e3:.1f} M tokens/s")
+    assert all(torch.isfinite(o.float()).all() for o in out)

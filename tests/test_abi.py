@@ -101,3 +101,23 @@ def test_compute_calls_validate_before_touching_the_device(lib):
     # workspace too small
     assert lib.tree_attn_bwd(p.handle, fake, fake, fake, fake, fake, fake, fake, fake, fake,
                              2, 2, 64, 1.0, fake, 16, None) == -6
+
+
+def test_linear_calls_validate_on_the_host(lib):
+    """The linear-attention calls refuse bad arguments before any device work."""
+    p = TreePlan([-1, 0], [100, 60])
+    fake, odd = C.c_void_p(0x1000), C.c_void_p(0x1008)
+    f7 = [fake] * 7
+    bwd = lib.tree_attn_linear_bwd
+    fwd = lib.tree_attn_linear_fwd
+    assert bwd(p.handle, None, *f7[:6], fake, 2, 1, 128, 1.0, fake, 1 << 30, None) == -1      # null tensor
+    assert bwd(p.handle, *f7, None, 2, 1, 128, 1.0, fake, 1 << 30, None) == -1                # null decay
+    assert bwd(p.handle, *f7, fake, 3, 2, 128, 1.0, fake, 1 << 30, None) == -1                # hq % hkv != 0
+    assert bwd(p.handle, *f7, fake, 2, 1, 64, 1.0, fake, 1 << 30, None) == -4                 # d != 128
+    assert bwd(p.handle, *f7, fake, 2, 1, 128, 0.0, fake, 1 << 30, None) == -1                # scale <= 0
+    assert bwd(p.handle, *f7, fake, 2, 1, 128, float("inf"), fake, 1 << 30, None) == -1
+    assert bwd(p.handle, odd, *f7[:6], fake, 2, 1, 128, 1.0, fake, 1 << 30, None) == -5      # misaligned q
+    assert bwd(p.handle, *f7[:6], odd, fake, 2, 1, 128, 1.0, fake, 1 << 30, None) == -5      # misaligned dv
+    assert fwd(p.handle, None, fake, fake, fake, fake, 2, 1, 128, 1.0, fake, 1 << 30, None) == -1
+    assert fwd(p.handle, fake, fake, fake, fake, fake, 2, 1, 64, 1.0, fake, 1 << 30, None) == -4
+    assert fwd(p.handle, fake, fake, odd, fake, fake, 2, 1, 128, 1.0, fake, 1 << 30, None) == -5

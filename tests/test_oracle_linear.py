@@ -130,3 +130,20 @@ def test_backward_recurrent_equals_parallel(seed):
     b = OLN.backward_recurrent(t.parent, t.seg_len, q, k, v, do, dec, 0.7)
     for x, y in zip(a, b):
         assert np.abs(x - y).max() <= 1e-10 * max(1.0, np.abs(x).max())
+
+
+def test_backward_chain_no_decay_equals_torch_autograd():
+    """A single chain with gamma = 1 is causal linear attention, scale * tril(Q K^T) V:
+    its gradients from torch autograd equal the oracle's backward."""
+    t = WT.chain_tree([6, 5])
+    q, k, v = rnd(t.n_tokens, 2, 1, 4, 21)
+    do = np.random.default_rng(22).normal(size=(t.n_tokens, 2, 4))
+    s = 0.45
+    dq, dk, dv = OLN.backward_parallel(t.parent, t.seg_len, q, k, v, do, [1.0], s)
+    Q = torch.tensor(q, dtype=torch.float64, requires_grad=True)
+    K = torch.tensor(k, dtype=torch.float64, requires_grad=True)
+    V = torch.tensor(v, dtype=torch.float64, requires_grad=True)
+    out = torch.stack([s * torch.tril(Q[:, h] @ K[:, 0].T) @ V[:, 0] for h in range(2)], dim=1)
+    (out * torch.tensor(do)).sum().backward()
+    for mine, ref in ((dq, Q.grad), (dk, K.grad), (dv, V.grad)):
+        assert np.abs(mine - ref.numpy()).max() < 1e-12

@@ -638,7 +638,7 @@ def run_extras(args):
     del logits
 
     # linear attention over the tree (chunks of <= 128 tokens, state handed to children)
-    from prefix_tree_attention_attn_gb300.linear import linear_workspace, tree_linear_fwd
+    from prefix_tree_attention_attn_gb300.linear import linear_workspace, tree_linear_bwd, tree_linear_fwd
     for wname in ("grpo_star",) if args.extras_small else ("grpo_star", "long_context"):
         tl = WT.load_tree(wname)
         hl, rl = WX.HEADS[wname], WX.VALUE_RECIPES[wname]
@@ -660,7 +660,23 @@ def run_extras(args):
                                        "frac": flops / ms / 1e9 / measured_peaks()[0]},
                           "config": {"workload": wname, "chunks": nc, "hq": hl.hq, "hkv": hl.hkv, "d": hl.d,
                                      "decay": 0.999, "workspace_bytes": wsb}, "dtype": "bf16"}))
-        del xl, ws, ol
+        dql, dkl, dvl = torch.empty_like(xl["q"]), torch.empty_like(xl["k"]), torch.empty_like(xl["v"])
+        runb = lambda: tree_linear_bwd(pl, xl["q"], xl["k"], xl["v"], xl["do"], dec, 1 / math.sqrt(hl.d), dq=dql,
+                                       dk=dkl, dv=dvl, workspace=ws)
+        msb = timed(runb, iters=10 if wname == "grpo_star" else 3, warm=2)
+        # tensor work issued: dQ is the forward's; F per chunk and q-head Q^T dO (2 d^2 128);
+        # per chunk and kv-head V Rsum^T and K Rsum (2 x 2 x 128 d^2); per chunk and
+        # q-head K Q^T, V dO^T, P^T dO and dA^T Q (4 x 2 x 128 x 128 x d)
+        flops_b = flops + nc * (hl.hq * 2 * hl.d * hl.d * 128 + hl.hkv * 4 * 128 * hl.d * hl.d
+                                + hl.hq * 4 * 2 * 128 * 128 * hl.d)
+        print(json.dumps({"metric": "tree linear attention backward (dQ, dK, dV; adjoint state summed over children)",
+                          "value": tl.n_tokens / (msb / 1e3), "unit": "compact tokens/s", "ms": msb,
+                          "roofline": {"bound": "tensor", "achieved": flops_b / msb / 1e9, "unit": "TFLOP/s",
+                                       "peak": measured_peaks()[0],
+                                       "frac": flops_b / msb / 1e9 / measured_peaks()[0]},
+                          "config": {"workload": wname, "chunks": nc, "hq": hl.hq, "hkv": hl.hkv, "d": hl.d,
+                                     "decay": 0.999}, "dtype": "bf16"}))
+        del xl, ws, ol, dql, dkl, dvl
 
     ta = WT.load_tree("agentic_tree")
     pa = TreePlan(ta.parent, ta.seg_len)

@@ -64,6 +64,8 @@ extern "C" {
 #define TREE_ATTN_ERR_DEVICE_TIMEOUT -10  /* a bounded device wait ran out        */
 #define TREE_ATTN_ERR_SCRATCH_TOO_SMALL -11 /* tree_attn_bwd_noalloc: the problem
                                              needs more than its fixed scratch    */
+#define TREE_ATTN_ERR_INVALID_DECAY  -12  /* device status only: a linear-attention
+                                             decay outside (0, 1]                 */
 
 /* ---- tile classes (tree_attn_plan_export) ------------------------------- */
 #define TREE_ATTN_TILE_FULL     1   /* every valid (query, key) pair attended  */
@@ -143,7 +145,14 @@ int tree_attn_workspace_size(tree_attn_plan_t plan, int32_t hq, int32_t hkv, int
 
 /* Forward: O and LSE (see the formulas above).  softmax_scale (> 0, finite)
  * is applied to the logits (pass 1/sqrt(d) for standard attention).  d in {64, 128}.  The
- * forward needs no workspace (pass NULL, 0).  Work is queued on `stream`. */
+ * forward needs no workspace (pass NULL, 0).  Work is queued on `stream`.
+ * Section: AReaL-DTA abstract (each shared prefix computed once in the forward
+ * pass, with every trajectory's result unchanged); HARTS abstract (attention
+ * over compact tokens of an arbitrary rollout tree, equal to per-trajectory
+ * training).  Only the kv-tiles on a q-tile's ancestor list are loaded.
+ * Errors: INVALID_ARG (null pointer, scale not finite or <= 0), UNSUPPORTED
+ * (head layout), TOO_LARGE, ALIGNMENT, NO_DEVICE, OUT_OF_MEMORY (the plan's
+ * first upload), CUDA (launch). */
 int tree_attn_fwd(tree_attn_plan_t plan, const void* q, const void* k, const void* v,
                   void* o, float* lse, int32_t hq, int32_t hkv, int32_t d,
                   float softmax_scale, void* workspace, size_t ws_bytes, void* stream);
@@ -152,7 +161,13 @@ int tree_attn_fwd(tree_attn_plan_t plan, const void* q, const void* k, const voi
  * the workspace tree_attn_workspace_size reports (device memory, 256-byte
  * aligned, contents on entry ignored).  dK and dV are reduced over a kv-tile's
  * descendant q-tiles in a fixed order, so they are bitwise reproducible; dQ is
- * accumulated with fp32 atomics, so its last bits may vary run to run. */
+ * accumulated with fp32 atomics, so its last bits may vary run to run.
+ * Section: AReaL-DTA abstract and HARTS abstract (the backward pass too
+ * computes each shared prefix once, and every trajectory gets the gradients
+ * training it alone would give).  dout is the compact gradient of one scalar
+ * loss (per-trajectory weights already folded in, e.g. tree_attn_scale_rows).
+ * Errors as tree_attn_fwd, plus WORKSPACE (missing or smaller than reported;
+ * ALIGNMENT when not 256-byte aligned). */
 int tree_attn_bwd(tree_attn_plan_t plan, const void* q, const void* k, const void* v,
                   const void* o, const float* lse, const void* dout,
                   void* dq, void* dk, void* dv, int32_t hq, int32_t hkv, int32_t d,
@@ -190,9 +205,13 @@ int tree_attn_bwd_stages(tree_attn_plan_t plan, const void* q, const void* k, co
  *    GPU (different streams, or different host threads) race on it; serialise
  *    them, e.g. on one stream.  Each call overwrites the array before reading
  *    it, so nothing from an earlier call leaks into the result.
- *  - The first call on a device looks up the array's device address.  The call
- *    copies the plan tables from host memory (a short synchronous staging of a
- *    few kilobytes) and calls no cudaMalloc, cudaFree or allocating routine.
+ *  - The first call on a device looks up the array's device address.  Each
+ *    call copies the plan tables into the array from pageable host memory:
+ *    4 bytes per token (rounded up to a multiple of 128 tokens), 4 per q-tile
+ *    and 16 per backward work item, e.g. 45 KB for an 11k-token tree.  A copy
+ *    from pageable memory is staged through the driver before the call returns,
+ *    so the host waits for it.  The call makes no cudaMalloc, cudaFree or other
+ *    allocating call.
  * Arguments, layouts, stream semantics and the other status codes are those of
  * tree_attn_bwd. */
 int tree_attn_bwd_noalloc(tree_attn_plan_t plan, const void* q, const void* k, const void* v,
@@ -205,9 +224,11 @@ size_t tree_attn_noalloc_scratch_bytes(void);
 
 /* Synchronise `stream`, then read and clear the device status word of the
  * current device: 0 when every kernel's bounded waits finished in time,
- * otherwise TREE_ATTN_ERR_DEVICE_TIMEOUT - 1000 * (site of the wait) or
- * TREE_ATTN_ERR_ALIGNMENT (shared memory misaligned).  Kernels that hit such
- * an error return early and leave their outputs incomplete. */
+ * otherwise TREE_ATTN_ERR_DEVICE_TIMEOUT - 1000 * (site of the wait),
+ * TREE_ATTN_ERR_ALIGNMENT (shared memory misaligned) or
+ * TREE_ATTN_ERR_INVALID_DECAY (tree_linear.h: a decay outside (0, 1]).  The
+ * first error recorded wins.  Kernels that hit a failed wait return early and
+ * leave their outputs incomplete. */
 int tree_attn_get_device_status(void* stream);
 
 /* Self-test of the kernels' failure path: launches one thread that waits on a

@@ -27,7 +27,11 @@
  * (three tensor-core products, the decay mask in registers).
  *
  * Tensors as in tree_attn.h: Q, O [N, hq, d] bf16, K, V [N, hkv, d] bf16 in
- * packed order; decay fp32 [hkv] (device).  d = 128.  The workspace holds the
+ * packed order; decay fp32 [hkv] (device), every entry in (0, 1].  The decay
+ * lives on the device, so the host cannot check it: a value outside (0, 1]
+ * (0, negative, above 1, NaN) records TREE_ATTN_ERR_INVALID_DECAY in the
+ * device status word (tree_attn_get_device_status) and leaves the call's
+ * outputs undefined.  d = 128.  The workspace holds the
  * per-chunk increments and entering states and the per-node exit states
  * (fp32); contents on entry ignored.  Asynchronous on `stream`.
  */

@@ -148,23 +148,34 @@ def tree_attn_bwd(plan: TreePlan, q, k, v, o, lse, dout, softmax_scale: float, d
     backward (``tree_attn_bwd_stages``); stages must run in order with one
     workspace."""
     import torch
-    N, hq, d = q.shape
+    _, hq, d = q.shape
     hkv = k.shape[1]
-    for name, t, shp, dt in (("q", q, (N, hq, d), torch.bfloat16), ("k", k, (N, hkv, d), torch.bfloat16),
-                             ("v", v, (N, hkv, d), torch.bfloat16), ("o", o, (N, hq, d), torch.bfloat16),
-                             ("lse", lse, (hq, N), torch.float32), ("dout", dout, (N, hq, d), torch.bfloat16)):
-        _check_tensor(t, name, shp, dt)
+    N = plan.n_tokens
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    _check_bwd_tensors(N, hq, hkv, d, q=q, k=k, v=v, o=o, lse=lse, dout=dout, dq=dq, dk=dk, dv=dv)
     _, need = plan.workspace_size(hq, hkv, d)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
-    B.check(B.load().tree_attn_bwd_stages(plan.handle, _dptr(q), _dptr(k), _dptr(v), _dptr(o), _dptr(lse),
-                                          _dptr(dout), _dptr(dq), _dptr(dk), _dptr(dv), hq, hkv, d,
-                                          float(softmax_scale), _dptr(workspace), workspace.numel(),
-                                          _stream_ptr(stream), int(stages)), "tree_attn_bwd_stages")
+    args = (plan.handle, _dptr(q), _dptr(k), _dptr(v), _dptr(o), _dptr(lse), _dptr(dout), _dptr(dq), _dptr(dk),
+            _dptr(dv), hq, hkv, d, float(softmax_scale), _dptr(workspace), workspace.numel(), _stream_ptr(stream))
+    if int(stages) == BWD_PRE | BWD_MAIN | BWD_POST:
+        B.check(B.load().tree_attn_bwd(*args), "tree_attn_bwd")
+    else:
+        B.check(B.load().tree_attn_bwd_stages(*args, int(stages)), "tree_attn_bwd_stages")
     return dq, dk, dv
+
+
+def _check_bwd_tensors(N, hq, hkv, d, **t):
+    """Every backward tensor against the plan's token count N and the head
+    layout, before anything is launched (the library sizes its reads and
+    writes from the plan)."""
+    import torch
+    shapes = {"q": (N, hq, d), "k": (N, hkv, d), "v": (N, hkv, d), "o": (N, hq, d), "lse": (hq, N),
+              "dout": (N, hq, d), "dq": (N, hq, d), "dk": (N, hkv, d), "dv": (N, hkv, d)}
+    for name, x in t.items():
+        _check_tensor(x, name, shapes[name], torch.float32 if name == "lse" else torch.bfloat16)
 
 
 def tree_attn_bwd_noalloc(plan: TreePlan, q, k, v, o, lse, dout, softmax_scale: float, dq, dk, dv, stream=None):
@@ -175,15 +186,9 @@ def tree_attn_bwd_noalloc(plan: TreePlan, q, k, v, o, lse, dout, softmax_scale: 
     fixed scratch (``noalloc_scratch_bytes()``) bounds the problem size, and
     calls that overlap on the GPU share that scratch, so run them one after
     another."""
-    import torch
-    N, hq, d = q.shape
+    _, hq, d = q.shape
     hkv = k.shape[1]
-    for name, t, shp, dt in (("q", q, (N, hq, d), torch.bfloat16), ("k", k, (N, hkv, d), torch.bfloat16),
-                             ("v", v, (N, hkv, d), torch.bfloat16), ("o", o, (N, hq, d), torch.bfloat16),
-                             ("lse", lse, (hq, N), torch.float32), ("dout", dout, (N, hq, d), torch.bfloat16),
-                             ("dq", dq, (N, hq, d), torch.bfloat16), ("dk", dk, (N, hkv, d), torch.bfloat16),
-                             ("dv", dv, (N, hkv, d), torch.bfloat16)):
-        _check_tensor(t, name, shp, dt)
+    _check_bwd_tensors(plan.n_tokens, hq, hkv, d, q=q, k=k, v=v, o=o, lse=lse, dout=dout, dq=dq, dk=dk, dv=dv)
     B.check(B.load().tree_attn_bwd_noalloc(plan.handle, _dptr(q), _dptr(k), _dptr(v), _dptr(o), _dptr(lse),
                                            _dptr(dout), _dptr(dq), _dptr(dk), _dptr(dv), hq, hkv, d,
                                            float(softmax_scale), _stream_ptr(stream)), "tree_attn_bwd_noalloc")

@@ -61,29 +61,12 @@ int make_tmap(CUtensorMap* m, const void* base, int64_t rows, int heads, int d, 
     return r == CUDA_SUCCESS ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
 }
 
-// Backward tensor-core pass.  head_dim 128: the full-step kernel (every MMA at
-// N = 128), or with TREE_ATTN_BWD128=0 at build time the half-step ping-pong
-// kernel.  head_dim 64: the general kernel.
-#ifndef TREE_ATTN_BWD128
-#define TREE_ATTN_BWD128 1
-#endif
+// Backward tensor-core pass: the full-step kernel for head_dim 128 (every MMA
+// at N = 128), the general kernel for head_dim 64.
 int launch_main(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                const CUtensorMap& tdq, const void* q, const void* dout, void* dq_acc, int64_t N, int hq,
-                const BwdParams& p, int grid, cudaStream_t s) {
-    cudaError_t e;
-    if (d == 128 && TREE_ATTN_BWD128 == 0) {
-        // 64-row boxes: Q / dO half tiles and dQ^T half tiles of the ping-pong kernel
-        CUtensorMap tq64, tdo64, tdq64;
-        int st;
-        if ((st = make_tmap(&tq64, q, N, hq, d, false, 64)) || (st = make_tmap(&tdo64, dout, N, hq, d, false, 64)) ||
-            (st = make_tmap(&tdq64, dq_acc, N, hq, d, true, 64)))
-            return st;
-        e = launch_bwd_pp(&tq, &tk, &tv, &tdo, &tdq64, &tq64, &tdo64, p, grid, s);
-    } else if (d == 128) {
-        e = launch_bwd_fs(&tq, &tk, &tv, &tdo, &tdq, p, grid, s);
-    } else {
-        e = launch_bwd(d, &tq, &tk, &tv, &tdo, &tdq, p, grid, s);
-    }
+                const CUtensorMap& tdq, const BwdParams& p, int grid, cudaStream_t s) {
+    const cudaError_t e = d == 128 ? launch_bwd_fs(&tq, &tk, &tv, &tdo, &tdq, p, grid, s)
+                                   : launch_bwd(d, &tq, &tk, &tv, &tdo, &tdq, p, grid, s);
     return e == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
 }
 
@@ -395,7 +378,7 @@ int tree_attn_bwd_stages(tree_attn_plan_t P, const void* q, const void* k, const
     const int64_t n_items = (int64_t)P->bwd_items.size() / 4;
     if (n_items * hkv > INT32_MAX) return TREE_ATTN_ERR_TOO_LARGE;
     if (stages & TREE_ATTN_BWD_MAIN) {
-        if ((st = launch_main(d, tq, tk, tv, tdo, tdq, q, dout, ws + w.dq_acc, P->N, hq, p, (int)(n_items * hkv), s)))
+        if ((st = launch_main(d, tq, tk, tv, tdo, tdq, p, (int)(n_items * hkv), s)))
             return st;
     }
 
@@ -533,7 +516,7 @@ int tree_attn_bwd_noalloc(tree_attn_plan_t P, const void* q, const void* k, cons
     p.scale = softmax_scale;
     p.scale_log2 = softmax_scale * 1.4426950408889634f;
     p.status = status;
-    if ((st = launch_main(d, tq, tk, tv, tdo, tdq, q, dout, ws + w.dq_acc, P->N, hq, p, (int)(n_items * hkv), s)))
+    if ((st = launch_main(d, tq, tk, tv, tdo, tdq, p, (int)(n_items * hkv), s)))
         return st;
 
     BwdPostParams post;
@@ -604,8 +587,10 @@ const char* tree_attn_strerror(int s) {
         case TREE_ATTN_ERR_SCRATCH_TOO_SMALL:
             return "problem too large for the fixed scratch of tree_attn_bwd_noalloc "
                    "(see tree_attn_noalloc_scratch_bytes)";
+        case TREE_ATTN_ERR_DEVICE_TIMEOUT: return "a bounded device wait ran out";
+        case TREE_ATTN_ERR_INVALID_DECAY: return "linear-attention decay outside (0, 1]";
         default:
-            if (s <= TREE_ATTN_ERR_DEVICE_TIMEOUT) return "a bounded device wait ran out";
+            if (s <= TREE_ATTN_ERR_DEVICE_TIMEOUT - 1000) return "a bounded device wait ran out";
             return "unknown status";
     }
 }

@@ -64,9 +64,6 @@ cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t stream);
 cudaError_t launch_bwd(int d, const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                        const CUtensorMap* tdo, const CUtensorMap* tdq, const BwdParams& p, int grid,
                        cudaStream_t stream);
-cudaError_t launch_bwd_pp(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
-                          const CUtensorMap* tdo, const CUtensorMap* tdq64, const CUtensorMap* tq64,
-                          const CUtensorMap* tdo64, const BwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_bwd_fs(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv, const CUtensorMap* tdo,
                           const CUtensorMap* tdq, const BwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_bwd_post(const BwdPostParams& p, cudaStream_t stream);

@@ -54,6 +54,11 @@ __global__ void __launch_bounds__(160, 1)
     }
     const int chunk = blockIdx.x / hkv, g = blockIdx.x % hkv;
     const int off = chunks[4 * chunk], L = chunks[4 * chunk + 1];
+    // a decay outside (0, 1] has no meaning here (its log2 would be NaN or
+    // -inf); say so in the status word, once per kv-head (the call's outputs
+    // are then undefined)
+    if (chunk == 0 && threadIdx.x == 0 && !(decay[g] > 0.f && decay[g] <= 1.f))
+        report_status(status, TREE_ATTN_ERR_INVALID_DECAY);
     const uint32_t b_full = sb, b_done = sb + 8, holder = sb + 16;
     const uint32_t ka = sb + 1024, va = ka + kTile;
     if (threadIdx.x == 0) {

@@ -24,8 +24,9 @@ def linear_workspace(plan: TreePlan, hkv: int, d: int):
 def tree_linear_fwd(plan: TreePlan, q, k, v, decay, scale: float, o=None, workspace=None, stream=None):
     """O [N, hq, d] bf16 = scale * sum over each token's path of gamma^(distance) (q.k) v."""
     import torch
-    N, hq, d = q.shape
+    _, hq, d = q.shape
     hkv = k.shape[1]
+    N = plan.n_tokens
     for name, t, shp in (("q", q, (N, hq, d)), ("k", k, (N, hkv, d)), ("v", v, (N, hkv, d))):
         _check_tensor(t, name, shp, torch.bfloat16)
     _check_tensor(decay, "decay", (hkv,), torch.float32)
@@ -44,8 +45,9 @@ def tree_linear_bwd(plan: TreePlan, q, k, v, do, decay, scale: float, dq=None, d
                     stream=None):
     """dQ [N, hq, d], dK / dV [N, hkv, d] bf16 for the compact output gradient dO."""
     import torch
-    N, hq, d = q.shape
+    _, hq, d = q.shape
     hkv = k.shape[1]
+    N = plan.n_tokens
     for name, t, shp in (("q", q, (N, hq, d)), ("k", k, (N, hkv, d)), ("v", v, (N, hkv, d)),
                          ("do", do, (N, hq, d))):
         _check_tensor(t, name, shp, torch.bfloat16)

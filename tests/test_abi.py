@@ -31,7 +31,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_status_codes_named(lib):
     text = open(HEADER).read()
     codes = {int(v) for v in re.findall(r"#define TREE_ATTN_(?:OK|ERR_[A-Z_]+)\s+(-?\d+)", text)}
-    assert codes == set(range(-11, 1))
+    assert codes == set(range(-12, 1))
     for code in codes:
         s = lib.tree_attn_strerror(code).decode()
         assert s and s != "unknown status"
@@ -121,3 +121,52 @@ def test_linear_calls_validate_on_the_host(lib):
     assert fwd(p.handle, None, fake, fake, fake, fake, 2, 1, 128, 1.0, fake, 1 << 30, None) == -1
     assert fwd(p.handle, fake, fake, fake, fake, fake, 2, 1, 64, 1.0, fake, 1 << 30, None) == -4
     assert fwd(p.handle, fake, fake, odd, fake, fake, 2, 1, 128, 1.0, fake, 1 << 30, None) == -5
+
+
+class FakeCudaTensor:
+    """Stands in for a device tensor so that the binding's host-side checks
+    run on a machine without a GPU; nothing is ever launched with it."""
+
+    def __init__(self, shape, dtype):
+        self.shape, self.dtype, self.is_cuda, self.device = tuple(shape), dtype, True, "cuda:0"
+
+    def is_contiguous(self):
+        return True
+
+    def data_ptr(self):
+        raise AssertionError("the binding reached a launch with a mismatched tensor")
+
+
+def test_tensors_must_match_the_plan_before_any_launch(lib):
+    """Every compute wrapper checks each tensor against the plan's token count
+    (the library sizes its reads and writes from the plan): a q shorter or
+    longer than the plan is refused with ValueError, before any launch."""
+    import torch
+    from prefix_tree_attention_attn_gb300 import tree_attn_bwd, tree_attn_bwd_noalloc, tree_attn_fwd
+    from prefix_tree_attention_attn_gb300.linear import tree_linear_bwd, tree_linear_fwd
+    p = TreePlan([-1, 0], [100, 60])          # 160 tokens
+    hq, hkv, d = 4, 2, 128
+    bf, f32 = torch.bfloat16, torch.float32
+    for n_q in (159, 161, 320):
+        def t(n, h):
+            return FakeCudaTensor((n, h, d), bf)
+        good_q, bad_q = t(160, hq), t(n_q, hq)
+        kk, vv = t(160, hkv), t(160, hkv)
+        lse = FakeCudaTensor((hq, 160), f32)
+        outs = dict(dq=t(160, hq), dk=t(160, hkv), dv=t(160, hkv))
+        with pytest.raises(ValueError):
+            tree_attn_fwd(p, bad_q, kk, vv, 1.0, o=t(n_q, hq), lse=FakeCudaTensor((hq, n_q), f32))
+        with pytest.raises(ValueError):
+            tree_attn_bwd(p, bad_q, kk, vv, t(n_q, hq), lse, t(n_q, hq), 1.0, workspace=good_q, **outs)
+        with pytest.raises(ValueError):      # right q, short dout
+            tree_attn_bwd(p, good_q, kk, vv, good_q, lse, t(n_q, hq), 1.0, workspace=good_q, **outs)
+        with pytest.raises(ValueError):      # right inputs, dq of another length
+            tree_attn_bwd(p, good_q, kk, vv, good_q, lse, good_q, 1.0, dq=t(n_q, hq), dk=outs["dk"],
+                          dv=outs["dv"], workspace=good_q)
+        with pytest.raises(ValueError):
+            tree_attn_bwd_noalloc(p, bad_q, kk, vv, t(n_q, hq), lse, t(n_q, hq), 1.0, **outs)
+        dec = FakeCudaTensor((hkv,), f32)
+        with pytest.raises(ValueError):
+            tree_linear_fwd(p, bad_q, kk, vv, dec, 1.0, o=t(n_q, hq), workspace=good_q)
+        with pytest.raises(ValueError):
+            tree_linear_bwd(p, bad_q, kk, vv, t(n_q, hq), dec, 1.0, workspace=good_q, **outs)

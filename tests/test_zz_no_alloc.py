@@ -1,57 +1,79 @@
-"""The allocation-free backward (tree_attn_bwd_noalloc) against the regular one.
+"""The allocation-free backward (tree_attn_bwd_noalloc), checked at the source.
 
 tree_attn_bwd_noalloc serves callers that cannot allocate device memory where
-they run the backward -- their memory belongs to another allocator, or an
-allocation could synchronise the device, or they work to a fixed budget.  It
-keeps its scratch in one fixed device array of the library.  These tests call
-it through the C ABI twice in a row on the same inputs (the second call must
-not see anything left over from the first) and compare each result with the
-regular entry point's, under the backward tolerance of the parity tests.  The
-file sorts last so that a run stopping at the first failure has already run
-every other test.
+they run the backward: their device memory belongs to another allocator (a
+framework's caching pool), an allocation could synchronise the device, or they
+work to a fixed memory budget.  It keeps its plan tables and workspace in one
+fixed device array of the library, shared by every call.
+
+These tests call it through the C ABI several times in a row on different
+trees with nothing in between -- a larger problem first, then a smaller one
+with another head layout, then the first again -- so a call that read what the
+previous call left in the shared array would go wrong.  Each result is compared
+with the fp64 oracle under the backward tolerance of the parity tests, and
+with the regular entry point.  The file sorts last so that a run stopping at
+the first failure has already run every other test.
 """
 import numpy as np
 import pytest
 import torch
 
+from oracle import attention as OA
 from prefix_tree_attention_attn_gb300 import (TreePlan, device_status, noalloc_scratch_bytes, tree_attn_bwd,
                                               tree_attn_bwd_noalloc, tree_attn_fwd)
 from prefix_tree_attention_attn_gb300 import _binding as B
 from workloads import tensors as WX
 from workloads import trees as WT
 
+from .gpu_util import BWD_REL, rel_fro
+
 pytestmark = pytest.mark.gpu
 
-BWD_REL = 1e-2     # relative Frobenius error per tensor, as in the parity tests
-
-
-def rel(a, b):
-    a = a.float()
-    b = b.float()
-    return float((a - b).norm() / b.norm().clamp_min(1e-30))
-
-
-@pytest.mark.parametrize("parent,seg_len,hq,hkv,d", [
+# (parent, seg_len, hq, hkv, d): the first needs the most scratch
+CASES = [
     ([-1, 0, 0, 1], [150, 90, 40, 33], 4, 2, 128),
     ([-1, 0, 0, 2], [200, 129, 64, 7], 2, 1, 64),
-])
-def test_noalloc_matches_regular_backward_twice(lib, cuda_device, parent, seg_len, hq, hkv, d):
+]
+
+
+def prepare(case, seed, dev):
+    parent, seg_len, hq, hkv, d = case
     t = WT.Tree("noalloc", parent, seg_len)
-    x = WX.draw_inputs(t.n_tokens, WX.HeadConfig(hq, hkv, d), WX.ValueRecipe(1, 1, 1, 1, 1), seed=77)
+    x = WX.draw_inputs(t.n_tokens, WX.HeadConfig(hq, hkv, d), WX.ValueRecipe(1, 1, 1, 1, 1), seed=seed)
     scale = 1 / np.sqrt(d)
     plan = TreePlan(t.parent, t.seg_len)
-    q, k, v, do = (x[n].to(cuda_device) for n in ("q", "k", "v", "do"))
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
     o, lse = tree_attn_fwd(plan, q, k, v, scale)
-    ref = tree_attn_bwd(plan, q, k, v, o, lse, do, scale)
+    return {"t": t, "x": x, "scale": scale, "plan": plan, "dev": (q, k, v, o, lse, do)}
+
+
+def test_noalloc_back_to_back_calls_match_the_oracle(lib, cuda_device):
+    cases = [prepare(c, 77 + i, cuda_device) for i, c in enumerate(CASES)]
     torch.cuda.synchronize()
-    for call in range(2):
-        dq, dk, dv = (torch.full_like(a, float("nan")) for a in ref)
-        tree_attn_bwd_noalloc(plan, q, k, v, o, lse, do, scale, dq, dk, dv)
+    order = [0, 1, 0]
+    outs = []
+    for ci in order:                          # no synchronisation between the calls
+        c = cases[ci]
+        q, k, v, o, lse, do = c["dev"]
+        dq, dk, dv = (torch.full_like(a, float("nan")) for a in (q, k, v))
+        tree_attn_bwd_noalloc(c["plan"], q, k, v, o, lse, do, c["scale"], dq, dk, dv)
+        outs.append((dq, dk, dv))
+    torch.cuda.synchronize()
+    assert device_status() == 0
+    for ci, got in zip(order, outs):
+        c = cases[ci]
+        t, x = c["t"], c["x"]
+        want64 = OA.backward(t.parent, t.seg_len, x["q"], x["k"], x["v"], x["do"], c["scale"])
+        q, k, v, o, lse, do = c["dev"]
+        regular = tree_attn_bwd(c["plan"], q, k, v, o, lse, do, c["scale"])
         torch.cuda.synchronize()
-        assert device_status() == 0
-        for name, got, want in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
-            assert torch.isfinite(got.float()).all(), (call, name)
-            assert rel(got, want) <= BWD_REL, (call, name, rel(got, want))
+        for name, g, w64, wreg in zip(("dQ", "dK", "dV"), got, want64, regular):
+            gn = g.float().cpu().numpy()
+            assert np.isfinite(gn).all(), (ci, name)
+            e = rel_fro(gn, w64)
+            assert e <= BWD_REL, (ci, name, "vs oracle", e)
+            e2 = rel_fro(gn, wreg.float().cpu().numpy().astype(np.float64))
+            assert e2 <= BWD_REL, (ci, name, "vs tree_attn_bwd", e2)
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(lib, cuda_device):

@@ -1,11 +1,14 @@
 #!/usr/bin/env python
 """Benchmark: prefix-tree attention forward + backward on GB300.
 
-One step = one pass of the whole hot path over the synthetic GRPO-style star
-tree (a 1024-token prompt shared by 16 responses of U[256, 1024] tokens;
-32 query heads, 8 kv heads, head_dim 128, bf16): the forward kernel, then the
-backward's three stages.  The metric is useful TFLOP/s, counting only
-attended (ancestor) pairs: 4*d per pair and q-head forward, 10*d backward.
+One step = one pass of the whole hot path over one synthetic tree: the forward
+kernel, then the backward's three stages.  The default workload is the largest
+one, the long shared context (a 32,768-token prefix with 64 branches of 1-3
+segments of log-uniform length in [1024, 8192]; 64 query heads, 8 kv heads,
+head_dim 128, bf16; about 480k compact tokens).  The metric is useful TFLOP/s,
+counting only attended (ancestor) pairs: 4*d per pair and q-head forward, 10*d
+backward.  The same line also carries the smaller workloads (tiny binary tree,
+GRPO star, segment tree, agentic tree), each timed the same way.
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
 oracle instead, on a bounded sample of the same workload.
@@ -47,12 +50,13 @@ DESCRIPTIONS = {
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="grpo_star")
+    ap.add_argument("--workload", default="long_context")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-expanded", action="store_true")
+    ap.add_argument("--no-others", action="store_true", help="time the named workload only")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the CPU sample")
     ap.add_argument("--extras", action="store_true",
                     help="instead of the step, time the calls around it (tree batching, loss boundary, "
@@ -153,7 +157,13 @@ class ClockSampler:
 # the oracle on a bounded sample (CPU baseline and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_sample_step(tree, x, heads, scale, groups):
+# Workloads where one kv-group of the full expansion is too large for the host
+# (the long shared context: about 1e14 fp64 FLOP per kv-group) take the
+# row / key sample; the others take whole kv-groups.
+ROW_KEY_SAMPLE = {"long_context"}
+
+
+def oracle_group_step(tree, x, heads, scale, groups):
     """fp64 oracle forward + backward on kv-groups ``groups`` (their q-heads
     and kv-head) of the workload; returns the useful FLOPs it covers."""
     from oracle import attention as OA
@@ -172,21 +182,105 @@ def oracle_sample_step(tree, x, heads, scale, groups):
     return flops
 
 
-def cpu_baseline(tree, x, heads, scale, target_s):
-    """Time the oracle as it stands on one kv-group at a time until about
-    ``target_s`` seconds have been spent."""
+class RowKeySample:
+    """Rows and keys of one tree that the fp64 oracle evaluates one by one, on
+    kv-group 0 (q-heads 0..G-1, kv-head 0): O, LSE and dQ of a row over its own
+    root-to-node path, and dK, dV of a key near the end of a leaf segment over
+    its descendant queries.  Each is credited with its share of a full step's
+    useful FLOPs: 10*d per (row, key on its path) pair and q-head (forward 4*d;
+    S, dP and dQ of the backward 6*d) and 4*d per (key, descendant query) pair
+    and q-head (dV and dK).  Summed over every row and key of the tree these
+    shares give the step's 14*d*pairs*hq."""
+
+    ROWS_PER_STEP, KEYS_PER_STEP = 4, 1
+
+    def __init__(self, tree, d, G, seed=0):
+        import numpy as np
+        from oracle import layout as OL
+        self.tree, self.d, self.G = tree, d, G
+        order, off, N = OL.packed_layout(tree.parent, tree.seg_len)
+        self.N = N
+        self.tn = OL.token_nodes(tree.parent, tree.seg_len)
+        self.off = off
+        ch = OL.children(tree.parent)
+        self.above, self.sub_end = {}, {}
+        for u in order:
+            p = tree.parent[u]
+            self.above[u] = 0 if p < 0 else self.above[p] + tree.seg_len[p]
+        for u in reversed(order):
+            self.sub_end[u] = self.sub_end[ch[u][-1]] if ch[u] else int(off[u]) + tree.seg_len[u]
+        self.rng = np.random.default_rng(seed)
+        self.leaves = OL.leaves(tree.parent)
+
+    def path_len(self, i):
+        u = int(self.tn[i])
+        return self.above[u] + (i - int(self.off[u])) + 1
+
+    def descendants(self, j):
+        return self.sub_end[int(self.tn[j])] - j
+
+    def draw(self):
+        rows = sorted(int(r) for r in self.rng.choice(self.N, size=self.ROWS_PER_STEP, replace=False))
+        keys = []
+        for l in self.rng.choice(self.leaves, size=self.KEYS_PER_STEP, replace=False):
+            end = int(self.off[l]) + self.tree.seg_len[l]
+            keys.append(end - 1 - int(self.rng.integers(0, min(8, self.tree.seg_len[l]))))
+        return rows, sorted(keys)
+
+    def step(self, xg, scale):
+        """One bounded sample: returns the useful FLOPs credited to it."""
+        from oracle import attention as OA
+        t = self.tree
+        rows, keys = self.draw()
+        OA.forward_rows(t.parent, t.seg_len, xg["q"], xg["k"], xg["v"], scale, rows)
+        OA.backward_rows_dq(t.parent, t.seg_len, xg["q"], xg["k"], xg["v"], xg["do"], scale, rows)
+        OA.backward_keys_dkdv(t.parent, t.seg_len, xg["q"], xg["k"], xg["v"], xg["do"], scale, keys)
+        return self.d * self.G * (10.0 * sum(self.path_len(i) for i in rows)
+                                  + 4.0 * sum(self.descendants(j) for j in keys))
+
+    def describe(self):
+        return (f"fp64 oracle on kv-group 0 ({self.G} q-heads, 1 kv-head): per step O, LSE and dQ of "
+                f"{self.ROWS_PER_STEP} random rows over their root-to-node paths and dK, dV of "
+                f"{self.KEYS_PER_STEP} key(s) near a leaf end, credited 10*d per (row, path key) pair and 4*d per "
+                f"(key, descendant) pair per q-head")
+
+
+def group_slice(x, G):
+    """kv-group 0 of a tensor set, on the host (q-heads 0..G-1, kv-head 0)."""
+    return {"q": x["q"][:, :G].contiguous().cpu(), "k": x["k"][:, :1].contiguous().cpu(),
+            "v": x["v"][:, :1].contiguous().cpu(), "do": x["do"][:, :G].contiguous().cpu()}
+
+
+def cpu_baseline(name, tree, x, heads, scale, target_s):
+    """Time the oracle as it stands until about ``target_s`` seconds have been
+    spent: whole kv-groups one at a time, or row / key samples (ROW_KEY_SAMPLE)."""
     t0 = time.perf_counter()
-    flops, groups = 0.0, 0
-    while groups < heads.hkv:
-        flops += oracle_sample_step(tree, x, heads, scale, [groups])
-        groups += 1
-        if time.perf_counter() - t0 >= target_s:
-            break
-    dt = time.perf_counter() - t0
+    flops = 0.0
+    if name in ROW_KEY_SAMPLE:
+        xg = group_slice(x, heads.group)
+        smp = RowKeySample(tree, heads.d, heads.group)
+        t0 = time.perf_counter()
+        n = 0
+        while True:
+            flops += smp.step(xg, scale)
+            n += 1
+            if time.perf_counter() - t0 >= target_s:
+                break
+        dt = time.perf_counter() - t0
+        sample = f"{n} steps of: {smp.describe()}; {dt:.1f} s"
+    else:
+        groups = 0
+        while groups < heads.hkv:
+            flops += oracle_group_step(tree, x, heads, scale, [groups])
+            groups += 1
+            if time.perf_counter() - t0 >= target_s:
+                break
+        dt = time.perf_counter() - t0
+        sample = (f"fp64 numpy oracle, fwd+bwd of {groups} of {heads.hkv} kv-head groups "
+                  f"({groups * heads.group} q-heads) of the full tree, {dt:.1f} s")
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"fp64 numpy oracle, fwd+bwd of {groups} of {heads.hkv} kv-head groups "
-                      f"({groups * heads.group} q-heads) of the full tree, {dt:.1f} s; numpy BLAS default threads",
-            "cpu_model": cpu_model(), "blas_threads": blas_threads()}
+            "sample": sample + "; numpy BLAS default threads", "cpu_model": cpu_model(),
+            "blas_threads": blas_threads()}
 
 
 def cpu_model() -> str:
@@ -216,18 +310,29 @@ def run_reference(args):
     from workloads import tensors as WX
     from workloads import trees as WT
     tree = WT.load_tree(args.workload)
-    heads, rec, x = WX.workload_inputs(args.workload, tree.n_tokens)
+    heads, rec = WX.HEADS[base_name(args.workload)], WX.VALUE_RECIPES[args.workload]
+    if args.workload in ROW_KEY_SAMPLE:
+        # kv-group 0 drawn on the host with the workload's recipe and seed (the GPU
+        # arm draws this workload on the device)
+        xg = WX.draw_inputs(tree.n_tokens, WX.HeadConfig(heads.group, 1, heads.d), rec,
+                            1000 + WX.SEEDS[args.workload])
+        smp = RowKeySample(tree, heads.d, heads.group)
+        one = lambda: smp.step(xg, rec.scale)
+        sample = "per step: " + smp.describe()
+    else:
+        _, _, x = WX.workload_inputs(args.workload, tree.n_tokens)
+        one = lambda: oracle_group_step(tree, x, heads, rec.scale, [0])
+        sample = (f"fp64 numpy oracle fwd+bwd on kv-head group 0 ({heads.group} q-heads, 1 kv-head) of "
+                  f"the full tree per step")
     for _ in range(args.warmup):
-        oracle_sample_step(tree, x, heads, rec.scale, [0])
+        one()
     times, flops = [], 0.0
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        flops = oracle_sample_step(tree, x, heads, rec.scale, [0])
+        flops += one()
         times.append(time.perf_counter() - t0)
     total = sum(times)
-    value = flops * args.steps / total / 1e12
-    sample = (f"fp64 numpy oracle fwd+bwd on kv-head group 0 ({heads.group} q-heads, 1 kv-head) of "
-              f"the full tree per step")
+    value = flops / total / 1e12
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
@@ -244,6 +349,21 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # the GPU arm
 # ---------------------------------------------------------------------------
+
+DEFAULT_WORKLOAD = "long_context"
+# timed too, each in its own region, and reported inside the same line
+OTHER_WORKLOADS = ("tiny_binary", "grpo_star", "segment_tree", "agentic_tree")
+# drawn on the device (a CUDA generator with the workload's seed): the host
+# would take minutes for ~9e9 normal samples
+DEVICE_DRAWN = {"long_context"}
+# steps at least this long keep the tensor core busy for seconds: their
+# roofline takes the sustained bf16 peak, shorter ones the burst peak
+LONG_STEP_MS = 100.0
+
+
+def base_name(name: str) -> str:
+    return "tiny_binary" if name.startswith("tiny_binary") else name
+
 
 def max_over_ranks(local_ms: float, world: int, device=None) -> float:
     """The slowest rank's timed-region length (every rank runs its own tree;
@@ -284,6 +404,81 @@ def chain_batches(TA, lens, hq, hkv, d, budget_bytes):
         n_batches *= 2
 
 
+def device_inputs(WX, name, n_tokens, dev):
+    """Seeded bf16 Q, K, V, dO of a workload on the device."""
+    heads, rec = WX.HEADS[base_name(name)], WX.VALUE_RECIPES[name]
+    if name in DEVICE_DRAWN:
+        return heads, rec, WX.draw_inputs(n_tokens, heads, rec, 1000 + WX.SEEDS[name], device=str(dev),
+                                          chunk_rows=65536)
+    _, _, x = WX.workload_inputs(name, n_tokens)
+    return heads, rec, {n: t.to(dev) for n, t in x.items()}
+
+
+def timed_hot_path(torch, TA, plan, x, heads, scale, steps, warmup, flush, around=None):
+    """Warm up, then time ``steps`` steps (forward, backward pre / main / post)
+    with CUDA events on the launching stream, L2 flushed (untimed) before
+    each.  ``around`` = (enter, leave) callables wrapped round the timed
+    region.  Returns per-step [fwd, pre, main, post] milliseconds."""
+    hq, hkv, d = heads.hq, heads.hkv, heads.d
+    N = plan.n_tokens
+    q, k, v, do = x["q"], x["k"], x["v"], x["do"]
+    o = torch.empty_like(q)
+    lse = torch.empty((hq, N), dtype=torch.float32, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(max(plan.workspace_size(hq, hkv, d)[1], 1), dtype=torch.uint8, device=q.device)
+    stream = torch.cuda.current_stream()
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        TA.tree_attn_fwd(plan, q, k, v, scale, o=o, lse=lse)
+        for si, stage in enumerate((TA.BWD_PRE, TA.BWD_MAIN, TA.BWD_POST)):
+            if evs:
+                evs[1 + si].record(stream)
+            TA.tree_attn_bwd(plan, q, k, v, o, lse, do, scale, dq=dq, dk=dk, dv=dv, workspace=ws, stages=stage)
+        if evs:
+            evs[4].record(stream)
+
+    for _ in range(max(warmup, 3)):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    if TA.device_status() != 0:
+        raise RuntimeError("device status non-zero after warm-up")
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    if around:
+        around[0]()
+    torch.cuda.synchronize()
+    for kk in range(steps):
+        flush.fill_(kk & 0xff)             # evict L2 between timed steps (not timed)
+        step(evs[kk])
+    torch.cuda.synchronize()
+    if around:
+        around[1]()
+    status = TA.device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status}")
+    del o, lse, dq, dk, dv, ws
+    return [[e[i].elapsed_time(e[i + 1]) for i in range(4)] for e in evs]
+
+
+def stage_summary(per, f_fwd, f_bwd):
+    fwd_ms = statistics.mean(p[0] for p in per)
+    pre_ms = statistics.mean(p[1] for p in per)
+    main_ms = statistics.mean(p[2] for p in per)
+    post_ms = statistics.mean(p[3] for p in per)
+    step_ms = [sum(p) for p in per]
+    return {"ms_per_step": statistics.mean(step_ms), "ms_per_step_median": statistics.median(step_ms),
+            "fwd_ms": fwd_ms, "bwd_pre_ms": pre_ms, "bwd_main_ms": main_ms, "bwd_post_ms": post_ms,
+            "fwd_tflops": f_fwd / (fwd_ms / 1e3) / 1e12, "bwd_main_tflops": f_bwd / (main_ms / 1e3) / 1e12,
+            "tflops": (f_fwd + f_bwd) / (statistics.mean(step_ms) / 1e3) / 1e12}
+
+
+def launches_per_step(plan):
+    # forward, backward pre, backward main, dQ conversion, split dK/dV sum
+    return 4 + (1 if plan.info["n_split_kv_tiles"] > 0 else 0)
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -306,8 +501,9 @@ def run_ours(args):
         if world > 1:
             dist.barrier()
 
-    tree = WT.load_tree(args.workload)
-    heads, rec, x = WX.workload_inputs(args.workload, tree.n_tokens)
+    name = args.workload
+    tree = WT.load_tree(name)
+    heads, rec, x = device_inputs(WX, name, tree.n_tokens, dev)
     hq, hkv, d, scale = heads.hq, heads.hkv, heads.d, rec.scale
     t_plan = time.perf_counter()
     for _ in range(5):
@@ -317,95 +513,61 @@ def run_ours(args):
     N = plan.n_tokens
     f_fwd, f_bwd = useful_flops(plan.n_pairs, hq, d)
     flops_step = f_fwd + f_bwd
-
-    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
-    o = torch.empty_like(q)
-    lse = torch.empty((hq, N), dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws = torch.empty(max(plan.workspace_size(hq, hkv, d)[1], 1), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
-    n_splits = plan.info["n_split_kv_tiles"]
-    launches_per_step = 1 + 1 + 1 + 1 + (1 if n_splits > 0 else 0)
 
-    def step(evs=None):
-        if evs:
-            evs[0].record(stream)
-        TA.tree_attn_fwd(plan, q, k, v, scale, o=o, lse=lse)
-        if evs:
-            evs[1].record(stream)
-        TA.tree_attn_bwd(plan, q, k, v, o, lse, do, scale, dq=dq, dk=dk, dv=dv, workspace=ws,
-                         stages=TA.BWD_PRE)
-        if evs:
-            evs[2].record(stream)
-        TA.tree_attn_bwd(plan, q, k, v, o, lse, do, scale, dq=dq, dk=dk, dv=dv, workspace=ws,
-                         stages=TA.BWD_MAIN)
-        if evs:
-            evs[3].record(stream)
-        TA.tree_attn_bwd(plan, q, k, v, o, lse, do, scale, dq=dq, dk=dk, dv=dv, workspace=ws,
-                         stages=TA.BWD_POST)
-        if evs:
-            evs[4].record(stream)
-
-    for _ in range(max(args.warmup, 3)):
-        flush.fill_(1)
-        step()
-    torch.cuda.synchronize()
-    if TA.device_status() != 0:
-        raise RuntimeError("device status non-zero after warm-up")
-
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)                        # let the sampler start
-    barrier()
-    torch.cuda.synchronize()
-    wall0 = time.perf_counter()
-    for kk in range(args.steps):
-        flush.fill_(kk & 0xff)             # evict L2 between timed steps (not timed)
-        step(evs[kk])
-    torch.cuda.synchronize()
-    barrier()
-    wall = time.perf_counter() - wall0
-    clk = clocks.stop()
-    status = TA.device_status()
-    if status != 0:
-        raise RuntimeError(f"device status {status}")
+    wall = {}
 
-    per = [[e[i].elapsed_time(e[i + 1]) for i in range(4)] for e in evs]   # fwd, pre, main, post (ms)
-    step_ms = [sum(p) for p in per]
-    total_ms = sum(step_ms)
+    def enter():
+        clocks.start()
+        time.sleep(0.3)                    # let the sampler start
+        barrier()
+        torch.cuda.synchronize()
+        wall["t0"] = time.perf_counter()
+
+    def leave():
+        barrier()
+        wall["s"] = time.perf_counter() - wall["t0"]
+
+    per = timed_hot_path(torch, TA, plan, x, heads, scale, args.steps, args.warmup, flush, (enter, leave))
+    clk = clocks.stop()
+    summ = stage_summary(per, f_fwd, f_bwd)
+    total_ms = sum(sum(p) for p in per)
     total_max_ms = max_over_ranks(total_ms, world, dev)
     value = job_throughput(flops_step, args.steps, world, total_max_ms)
-    fwd_ms = statistics.mean(p[0] for p in per)
-    main_ms = statistics.mean(p[2] for p in per)
-    pre_ms = statistics.mean(p[1] for p in per)
-    post_ms = statistics.mean(p[3] for p in per)
 
     peak_burst, peak_sus, peak_src = measured_peaks()
+    long_step = summ["ms_per_step"] >= LONG_STEP_MS
+    peak = peak_sus if long_step else peak_burst
+    peak_name = f"{peak_src} bf16 {'sustained' if long_step else 'burst'}"
     # the backward's tensor-core kernel is bwd_fs_kernel (bwd_fs.cu) for d = 128, bwd_kernel (bwd.cu) else
     bwd_name, bwd_src = ("bwd_fs_kernel", "bwd_fs.cu") if d == 128 else ("bwd_kernel", "bwd.cu")
+    main_ms, fwd_ms = summ["bwd_main_ms"], summ["fwd_ms"]
     dominant = (bwd_name, main_ms, f_bwd, bwd_src) if main_ms >= fwd_ms else ("fwd_kernel", fwd_ms, f_fwd, "fwd.cu")
     achieved = dominant[2] / (dominant[1] / 1e3) / 1e12
     src_hash = kernel_source_hash([dominant[3], "ptx.cuh"])
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_burst, "unit": "TFLOP/s",
-                "frac": achieved / peak_burst, "traffic": recorded_traffic(dominant[0], args.workload, src_hash),
-                "kernel": dominant[0], "peak_source": f"{peak_src} bf16 burst",
-                "kernel_src_hash": src_hash}
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": recorded_traffic(dominant[0], name, src_hash),
+                "kernel": dominant[0], "peak_source": peak_name, "kernel_src_hash": src_hash,
+                "algorithmic": f"{'10' if dominant[0] != 'fwd_kernel' else '4'}*d*pairs*hq = {dominant[2]:.4g} FLOP "
+                               f"per launch / mean CUDA-event launch time {dominant[1]:.4g} ms"}
 
     # ---- end to end through the public API, host buffers ------------------
     e2e = None
     if rank == 0 or world > 1:
-        pin = {n: x[n].pin_memory() for n in ("q", "k", "v", "do")}
-        outs = {"o": torch.empty(o.shape, dtype=o.dtype, pin_memory=True),
-                "lse": torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True),
-                "dq": torch.empty(dq.shape, dtype=dq.dtype, pin_memory=True),
-                "dk": torch.empty(dk.shape, dtype=dk.dtype, pin_memory=True),
-                "dv": torch.empty(dv.shape, dtype=dv.dtype, pin_memory=True)}
+        pin = {n: torch.empty(x[n].shape, dtype=x[n].dtype, pin_memory=True) for n in ("q", "k", "v", "do")}
+        for n in pin:
+            pin[n].copy_(x[n])
+        outs = {"o": torch.empty((N, hq, d), dtype=torch.bfloat16, pin_memory=True),
+                "lse": torch.empty((hq, N), dtype=torch.float32, pin_memory=True),
+                "dq": torch.empty((N, hq, d), dtype=torch.bfloat16, pin_memory=True),
+                "dk": torch.empty((N, hkv, d), dtype=torch.bfloat16, pin_memory=True),
+                "dv": torch.empty((N, hkv, d), dtype=torch.bfloat16, pin_memory=True)}
         h2d = sum(t_.numel() * t_.element_size() for t_ in pin.values())
         d2h = sum(t_.numel() * t_.element_size() for t_ in outs.values())
-        e2e_steps = max(3, min(args.steps, 20))
-
+        # a bounded number of end-to-end steps: about 20 s at most
+        e2e_steps = max(2, min(args.steps, 20, int(20e3 / (1.5 * summ["ms_per_step"] + 1.0))))
+        e2e_warm = 1 if long_step else max(3, args.warmup)
         side = torch.cuda.Stream(device=dev)        # copies that can overlap compute
 
         def e2e_step():
@@ -425,12 +587,12 @@ def run_ours(args):
                 side.wait_event(fwd_done)
                 outs["o"].copy_(oo, non_blocking=True)
                 outs["lse"].copy_(ll, non_blocking=True)
-            for name, src in (("dq", a), ("dk", b), ("dv", c)):
-                outs[name].copy_(src, non_blocking=True)
+            for nm, src in (("dq", a), ("dk", b), ("dv", c)):
+                outs[nm].copy_(src, non_blocking=True)
             torch.cuda.synchronize(dev)      # the step's results are on the host
             p2.close()
 
-        for _ in range(max(3, args.warmup)):   # first-touch costs: pinned pages, allocator pools
+        for _ in range(e2e_warm):   # first-touch costs: allocator pools, plan upload
             e2e_step()
         barrier()
         t0 = time.perf_counter()
@@ -438,15 +600,17 @@ def run_ours(args):
             e2e_step()
         e2e_s = (time.perf_counter() - t0) / e2e_steps
         e2e = {"value": flops_step * world / e2e_s / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3, "steps": e2e_steps,
                "includes": "host plan build + device upload, H2D of q/k/v/dO from pinned memory, fwd+bwd, "
                            "D2H of o/lse/dq/dk/dv; dO arrives during the forward and O/LSE leave during the "
                            "backward (side stream)"}
+        del pin, outs
+        torch.cuda.empty_cache()
 
     # ---- same kernels on the expanded trajectories ---------------------------
-    # Every root-to-leaf trajectory as its own chain. When the whole expanded
+    # Every root-to-leaf trajectory as its own chain.  When the whole expanded
     # forest does not fit in half of the free device memory (the long shared
-    # context: ~2.6 M tokens), the chains run in equal batches one after another
+    # context: ~2.5 M tokens), the chains run in equal batches one after another
     # inside each timed step, and the step time is the sum.
     expanded = None
     if not args.no_expanded and rank == 0:
@@ -469,11 +633,11 @@ def run_ours(args):
                 oo, ll = TA.tree_attn_fwd(pb, qb, kb, vb, scale)
                 TA.tree_attn_bwd(pb, qb, kb, vb, oo, ll, dob, scale, workspace=wse)
 
-        for _ in range(3):
+        for _ in range(1 if long_step else 3):
             estep()
         torch.cuda.synchronize()
         ee = []
-        for _ in range(min(args.steps, 20)):
+        for _ in range(2 if long_step else min(args.steps, 20)):
             flush.fill_(3)
             a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a_.record()
@@ -482,15 +646,33 @@ def run_ours(args):
             ee.append((a_, b_))
         torch.cuda.synchronize()
         ems = statistics.mean(a_.elapsed_time(b_) for a_, b_ in ee)
-        expanded = {"ms_per_step": ems, "speedup": ems / (total_ms / args.steps), "n_tokens": Ne,
-                    "pairs": sum(pb.n_pairs for pb in eplans), "chain_batches": len(eplans)}
+        expanded = {"ms_per_step": ems, "speedup": ems / summ["ms_per_step"], "n_tokens": Ne,
+                    "pairs": sum(pb.n_pairs for pb in eplans), "chain_batches": len(eplans), "steps": len(ee)}
         for pb in eplans:
             pb.close()
         del xe, wse
+        torch.cuda.empty_cache()
+
+    # ---- the smaller workloads, each timed the same way ----------------------
+    others = []
+    if rank == 0 and world == 1 and name == DEFAULT_WORKLOAD and not args.no_others:
+        for wn in OTHER_WORKLOADS:
+            tw = WT.load_tree(wn)
+            hw, rw, xw = device_inputs(WX, wn, tw.n_tokens, dev)
+            pw = TA.TreePlan(tw.parent, tw.seg_len)
+            ff, fb = useful_flops(pw.n_pairs, hw.hq, hw.d)
+            pr = timed_hot_path(torch, TA, pw, xw, hw, rw.scale, min(args.steps, 20), 3, flush)
+            sw = stage_summary(pr, ff, fb)
+            sw.update({"name": wn, "workload": DESCRIPTIONS[wn], "n_tokens": pw.n_tokens, "pairs": pw.n_pairs,
+                       "hq": hw.hq, "hkv": hw.hkv, "d": hw.d, "steps": len(pr),
+                       "pct_peak": 100.0 * sw["tflops"] / peak_burst, "peak": f"{peak_src} bf16 burst"})
+            others.append(sw)
+            pw.close()
+            del xw
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(tree, x, heads, scale, args.cpu_seconds)
+        cpu = cpu_baseline(name, tree, x, heads, scale, args.cpu_seconds)
 
     if rank == 0:
         line = {
@@ -498,23 +680,26 @@ def run_ours(args):
             "warmup": max(args.warmup, 3), "ms_per_step": total_max_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": DESCRIPTIONS.get(args.workload, args.workload), "name": args.workload,
+            "config": {"workload": DESCRIPTIONS.get(name, name), "name": name,
                        "n_tokens": N, "pairs": plan.n_pairs, "hq": hq, "hkv": hkv, "d": d,
                        "softmax_scale": scale, "l2": "flushed between timed steps (512 MB write, untimed)",
+                       "inputs": "drawn on the device" if name in DEVICE_DRAWN else "drawn on the host, copied",
                        "parallelism": f"replicas x{world} (independent trees per GPU)"},
-            "pct_peak": 100.0 * value / world / peak_burst,
-            "ms_per_step_median": statistics.median(step_ms),
+            "pct_peak": 100.0 * value / world / peak, "peak_source": peak_name,
+            "ms_per_step_median": summ["ms_per_step_median"],
             "plan_ms_host": plan_ms,
-            "fwd_ms": fwd_ms, "bwd_pre_ms": pre_ms, "bwd_main_ms": main_ms, "bwd_post_ms": post_ms,
-            "fwd_tflops": f_fwd / (fwd_ms / 1e3) / 1e12, "bwd_main_tflops": f_bwd / (main_ms / 1e3) / 1e12,
+            "fwd_ms": summ["fwd_ms"], "bwd_pre_ms": summ["bwd_pre_ms"], "bwd_main_ms": summ["bwd_main_ms"],
+            "bwd_post_ms": summ["bwd_post_ms"], "fwd_tflops": summ["fwd_tflops"],
+            "bwd_main_tflops": summ["bwd_main_tflops"],
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": launches_per_step * args.steps,
+            "gpu_launches": launches_per_step(plan) * args.steps,
             "clocks": clk,
             "speedup_vs_expanded": expanded["speedup"] if expanded else None,
             "expanded": expanded,
-            "wall_s_timed_region": wall,
+            "other_workloads": others,
+            "wall_s_timed_region": wall.get("s"),
         }
         print(json.dumps(line))
     if world > 1:

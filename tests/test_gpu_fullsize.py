@@ -1,5 +1,20 @@
 """Full-size parity on the two largest workload trees (GPU).
 
+Element-wise, every row and key:
+
+* the agentic tree in full (all 32 q-heads on the GPU), with kv-group 0
+  (q-heads 0-3, kv-head 0) compared with the fp64 oracle on every token:
+  O, LSE and dQ of its q-heads, dK and dV of its kv-head -- the deep shared
+  turns' keys included;
+* a reduced long shared context: the same 32,768-token root with the first 4
+  branches of the long-context recipe (seed 5), one q-head and one kv-head, so
+  that the backward runs as on the full tree (q-range chunks doubled to 48
+  q-tiles, more than 2,048 partial dK/dV slots summed in a fixed order) and
+  every token's O, LSE, dQ, dK and dV -- the root's 32,768 keys included, each
+  summed over hundreds of descendant q-tiles -- is compared with the oracle.
+
+For the full trees, beyond those:
+
 The whole fp64 expansion is too expensive at these sizes (the long shared
 context expands to 2.5M tokens), so the oracle checks outputs it can compute
 one by one, exactly:
@@ -124,3 +139,71 @@ def test_agentic_tree_full_size():
 
 def test_long_context_full_size():
     check_workload("long_context", device_gen=True)
+
+
+def compare_all(tag, got, ref):
+    """Every element: O and LSE (max, mean abs), dQ, dK, dV (relative Frobenius)."""
+    out = {}
+    for name in ("o", "lse"):
+        e = np.abs(got[name].astype(np.float64) - ref[name])
+        out[name] = (float(e.max()), float(e.mean()))
+    for name in ("dq", "dk", "dv"):
+        out[name] = rel_fro(got[name], ref[name])
+    print(f"{tag}: O max/mean {out['o'][0]:.3e}/{out['o'][1]:.3e}, LSE max/mean "
+          f"{out['lse'][0]:.3e}/{out['lse'][1]:.3e}, rel Frobenius dQ {out['dq']:.3e} dK {out['dk']:.3e} "
+          f"dV {out['dv']:.3e}")
+    for name in ("o", "lse"):
+        assert np.isfinite(got[name]).all(), (tag, name)
+        assert out[name][0] <= FWD_MAX and out[name][1] <= FWD_MEAN, (tag, name, out[name])
+    for name in ("dq", "dk", "dv"):
+        assert np.isfinite(got[name]).all(), (tag, name)
+        assert out[name] <= BWD_REL, (tag, name, out[name])
+
+
+def oracle_all(t, q, k, v, do, scale):
+    ro, rl = OA.forward(t.parent, t.seg_len, q, k, v, scale)
+    rq, rk, rv = OA.backward(t.parent, t.seg_len, q, k, v, do, scale)
+    return {"o": ro, "lse": rl, "dq": rq, "dk": rk, "dv": rv}
+
+
+def test_agentic_tree_kv_group0_every_token():
+    """The whole agentic tree on the GPU; kv-group 0 against the oracle on
+    every token (about 2e12 useful fp64 FLOP on the host)."""
+    name = "agentic_tree"
+    t = WT.load_tree(name)
+    plan = TreePlan(t.parent, t.seg_len)
+    heads, rec, x = WX.workload_inputs(name, t.n_tokens)
+    G = heads.group
+    xd = {kk: vv.cuda() for kk, vv in x.items()}
+    o, lse, dq, dk, dv = run(plan, xd["q"], xd["k"], xd["v"], xd["do"], rec.scale)
+    got = {"o": o[:, :G].float().cpu().numpy(), "lse": lse[:G].cpu().numpy(),
+           "dq": dq[:, :G].float().cpu().numpy(), "dk": dk[:, :1].float().cpu().numpy(),
+           "dv": dv[:, :1].float().cpu().numpy()}
+    del xd, o, lse, dq, dk, dv
+    ref = oracle_all(t, x["q"][:, :G], x["k"][:, :1], x["v"][:, :1], x["do"][:, :G], rec.scale)
+    compare_all("agentic tree, kv-group 0, every token", got, ref)
+
+
+def test_long_context_reduced_every_token():
+    """32,768-token root + the first 4 branches of the long-context recipe, one
+    head: the backward's doubled chunk rule and > 2,048 partial slots in force,
+    every token compared with the oracle."""
+    t = WT.long_context_tree(seed=WX.SEEDS["long_context"], branches=4)
+    plan = TreePlan(t.parent, t.seg_len)
+    assert plan.info["bwd_chunk_qtiles"] > 24, plan.info
+    assert plan.info["n_partial_slots"] > 2048, plan.info
+    assert plan.info["n_split_kv_tiles"] >= 256          # every root kv-tile is split
+    rec = WX.VALUE_RECIPES["long_context"]
+    x = WX.draw_inputs(t.n_tokens, WX.HeadConfig(1, 1, 128), rec, 1000 + WX.SEEDS["long_context"])
+    xd = {kk: vv.cuda() for kk, vv in x.items()}
+    o, lse, dq, dk, dv = run(plan, xd["q"], xd["k"], xd["v"], xd["do"], rec.scale)
+    got = {"o": o.float().cpu().numpy(), "lse": lse.cpu().numpy(), "dq": dq.float().cpu().numpy(),
+           "dk": dk.float().cpu().numpy(), "dv": dv.float().cpu().numpy()}
+    ref = oracle_all(t, x["q"], x["k"], x["v"], x["do"], rec.scale)
+    compare_all(f"long context, root + 4 branches ({t.n_tokens} tokens), every token", got, ref)
+    # the root prefix's keys on their own: the ones summed over the most q-tiles
+    root = slice(0, t.seg_len[0])
+    for name in ("dk", "dv"):
+        e = rel_fro(got[name][root], ref[name][root])
+        print(f"  root-prefix {name}: rel Frobenius {e:.3e}")
+        assert e <= BWD_REL, (name, e)

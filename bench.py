@@ -44,6 +44,8 @@ DESCRIPTIONS = {
     "tiny_binary": "tiny binary tree 64 + 2x32 + 4x32 tokens; 2 heads, d=64",
     "long_context": "long shared context: 32768-token prefix + 64 chains of 1-3 log-U[1k,8k] segments; "
                     "64q/8kv heads, d=128",
+    "long_context_4b": "long shared context, first 4 of its 64 branches (58,232 tokens); 32q/4kv heads, d=128 "
+                       "(a few GB: the case profiler captures run on)",
 }
 
 
@@ -57,6 +59,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-expanded", action="store_true")
     ap.add_argument("--no-others", action="store_true", help="time the named workload only")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the CPU sample")
     ap.add_argument("--extras", action="store_true",
                     help="instead of the step, time the calls around it (tree batching, loss boundary, "
@@ -160,7 +163,7 @@ class ClockSampler:
 # Workloads where one kv-group of the full expansion is too large for the host
 # (the long shared context: about 1e14 fp64 FLOP per kv-group) take the
 # row / key sample; the others take whole kv-groups.
-ROW_KEY_SAMPLE = {"long_context"}
+ROW_KEY_SAMPLE = {"long_context", "long_context_4b"}
 
 
 def oracle_group_step(tree, x, heads, scale, groups):
@@ -355,7 +358,7 @@ DEFAULT_WORKLOAD = "long_context"
 OTHER_WORKLOADS = ("tiny_binary", "grpo_star", "segment_tree", "agentic_tree")
 # drawn on the device (a CUDA generator with the workload's seed): the host
 # would take minutes for ~9e9 normal samples
-DEVICE_DRAWN = {"long_context"}
+DEVICE_DRAWN = {"long_context", "long_context_4b"}
 # steps at least this long keep the tensor core busy for seconds: their
 # roofline takes the sustained bf16 peak, shorter ones the burst peak
 LONG_STEP_MS = 100.0
@@ -404,8 +407,17 @@ def chain_batches(TA, lens, hq, hkv, d, budget_bytes):
         n_batches *= 2
 
 
+def workload_tree(WT, name):
+    if name == "long_context_4b":     # the long-context recipe's first 4 branches
+        return WT.long_context_tree(seed=5, branches=4)
+    return WT.load_tree(name)
+
+
 def device_inputs(WX, name, n_tokens, dev):
     """Seeded bf16 Q, K, V, dO of a workload on the device."""
+    if name == "long_context_4b":
+        heads, rec = WX.HeadConfig(32, 4, 128), WX.VALUE_RECIPES["long_context"]
+        return heads, rec, WX.draw_inputs(n_tokens, heads, rec, 1005, device=str(dev), chunk_rows=65536)
     heads, rec = WX.HEADS[base_name(name)], WX.VALUE_RECIPES[name]
     if name in DEVICE_DRAWN:
         return heads, rec, WX.draw_inputs(n_tokens, heads, rec, 1000 + WX.SEEDS[name], device=str(dev),
@@ -502,7 +514,7 @@ def run_ours(args):
             dist.barrier()
 
     name = args.workload
-    tree = WT.load_tree(name)
+    tree = workload_tree(WT, name)
     heads, rec, x = device_inputs(WX, name, tree.n_tokens, dev)
     hq, hkv, d, scale = heads.hq, heads.hkv, heads.d, rec.scale
     t_plan = time.perf_counter()
@@ -554,7 +566,7 @@ def run_ours(args):
 
     # ---- end to end through the public API, host buffers ------------------
     e2e = None
-    if rank == 0 or world > 1:
+    if not args.no_e2e and (rank == 0 or world > 1):
         pin = {n: torch.empty(x[n].shape, dtype=x[n].dtype, pin_memory=True) for n in ("q", "k", "v", "do")}
         for n in pin:
             pin[n].copy_(x[n])

@@ -66,6 +66,8 @@ extern "C" {
                                              needs more than its fixed scratch    */
 #define TREE_ATTN_ERR_INVALID_DECAY  -12  /* device status only: a linear-attention
                                              decay outside (0, 1]                 */
+#define TREE_ATTN_ERR_DEVICE_BOUNDS  -13  /* device status only, debug builds: an
+                                             index failed its bounds check        */
 
 /* ---- tile classes (tree_attn_plan_export) ------------------------------- */
 #define TREE_ATTN_TILE_FULL     1   /* every valid (query, key) pair attended  */
@@ -226,7 +228,8 @@ size_t tree_attn_noalloc_scratch_bytes(void);
  * current device: 0 when every kernel's bounded waits finished in time,
  * otherwise TREE_ATTN_ERR_DEVICE_TIMEOUT - 1000 * (site of the wait),
  * TREE_ATTN_ERR_ALIGNMENT (shared memory misaligned) or
- * TREE_ATTN_ERR_INVALID_DECAY (tree_linear.h: a decay outside (0, 1]).  The
+ * TREE_ATTN_ERR_INVALID_DECAY (tree_linear.h: a decay outside (0, 1]), or in
+ * a debug build TREE_ATTN_ERR_DEVICE_BOUNDS - 1000 * (site of the check).  The
  * first error recorded wins.  Kernels that hit a failed wait return early and
  * leave their outputs incomplete. */
 int tree_attn_get_device_status(void* stream);
@@ -238,6 +241,26 @@ int tree_attn_get_device_status(void* stream);
  * attention kernels takes, with no fault and the context still usable.  Read
  * the result with tree_attn_get_device_status. */
 int tree_attn_selftest_wait_timeout(int32_t limit_ms, void* stream);
+
+/* Debug builds.  The library built with -DTREE_ATTN_DEBUG (libtreeattn_debug.so,
+ * made beside libtreeattn.so by the package's build) checks, in every attention
+ * kernel, the indices that come from the plan's tables and the tree's shape --
+ * work items, q-tile kv-tile lists, subtree ends of partial and ragged tiles,
+ * partial dK/dV slots, LSE / Delta rows, head numbers -- before they address
+ * global memory.  A failed check records TREE_ATTN_ERR_DEVICE_BOUNDS - 1000 *
+ * site in the device status word and the access is skipped or clamped to an
+ * in-range index, so nothing is read or written out of bounds; the results are
+ * then wrong, and the status says where.  (It stands in for a memory checker
+ * that cannot run on every machine.)  Release builds carry no checks.
+ * tree_attn_debug_checks() is 1 in a debug build, 0 otherwise. */
+int tree_attn_debug_checks(void);
+
+/* Self-test of the debug checks: one thread checks an index that is out of
+ * range on purpose, so a debug build records TREE_ATTN_ERR_DEVICE_BOUNDS -
+ * 1000 * 98 in the device status word (read it with
+ * tree_attn_get_device_status) and skips the access.  Release builds return
+ * TREE_ATTN_ERR_UNSUPPORTED and launch nothing. */
+int tree_attn_selftest_bounds(void* stream);
 
 /* Free the plan and its device copies (call after work using it finished). */
 void tree_attn_plan_destroy(tree_attn_plan_t plan);

@@ -1,6 +1,7 @@
 """ctypes declarations of the C ABI in include/*.h (marshalling only)."""
 from __future__ import annotations
 
+import contextlib
 import ctypes as C
 import os
 
@@ -54,6 +55,8 @@ SIGNATURES = {
     "tree_attn_noalloc_scratch_bytes": (C.c_size_t, []),
     "tree_attn_get_device_status": (C.c_int, [C.c_void_p]),
     "tree_attn_selftest_wait_timeout": (C.c_int, [C.c_int32, C.c_void_p]),
+    "tree_attn_debug_checks": (C.c_int, []),
+    "tree_attn_selftest_bounds": (C.c_int, [C.c_void_p]),
     "tree_attn_plan_destroy": (None, [C.c_void_p]),
     "tree_attn_strerror": (C.c_char_p, [C.c_int]),
     # include/tree_batch.h
@@ -103,6 +106,20 @@ def load(path: str = None) -> C.CDLL:
     if path == _build.LIB:
         _LIB = lib
     return lib
+
+
+@contextlib.contextmanager
+def library(path: str):
+    """Inside the block every call of the package goes to the library at
+    ``path`` -- e.g. ``build.LIB_DEBUG``, the same kernels with their bounds
+    checks compiled in.  Plans made inside the block belong to that library."""
+    global _LIB
+    saved = _LIB
+    _LIB = load(path)
+    try:
+        yield _LIB
+    finally:
+        _LIB = saved
 
 
 class TreeAttnError(RuntimeError):

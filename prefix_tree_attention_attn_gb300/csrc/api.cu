@@ -13,8 +13,11 @@
 
 namespace treeattn {
 
-// Device status word written by the kernels' bounded waits (0 = fine).
+// Device status word written by the kernels' bounded waits and, in debug
+// builds, their bounds checks (0 = fine).
 __device__ int g_device_status = 0;
+// Output word of the bounds self-test kernel.
+__device__ int g_selftest_word = 0;
 
 namespace {
 
@@ -103,10 +106,11 @@ int ensure_device(tree_attn_plan_s* P, DevicePlan** out) {
     const int64_t n_ent = (int64_t)P->qt_kv.size();
     const int64_t n_items = (int64_t)P->bwd_items.size() / 4;
     const int64_t n_splits = (int64_t)P->splits.size() / 4;
-    // one int32 buffer: subend | qt_ptr | qt_ent | fwd_order | kv_minsub | items | splits
-    const int64_t sizes[7] = {T * kBlock, T + 1, n_ent, T, T, 4 * n_items, 4 * std::max<int64_t>(n_splits, 1)};
-    int64_t offs[7], total = 0;
-    for (int k = 0; k < 7; ++k) {
+    // one int32 buffer: subend | qt_ptr | qt_ent | fwd_order | kv_minsub | items | splits | chunk_ptr
+    const int64_t sizes[8] = {T * kBlock, T + 1, n_ent, T, T, 4 * n_items, 4 * std::max<int64_t>(n_splits, 1),
+                              (int64_t)P->chunk_ptr.size()};
+    int64_t offs[8], total = 0;
+    for (int k = 0; k < 8; ++k) {
         offs[k] = total;
         total += (sizes[k] + 63) / 64 * 64;   // 256-byte aligned sections
     }
@@ -124,6 +128,7 @@ int ensure_device(tree_attn_plan_s* P, DevicePlan** out) {
     std::copy(P->kv_minsub.begin(), P->kv_minsub.end(), h.begin() + offs[4]);
     std::copy(P->bwd_items.begin(), P->bwd_items.end(), h.begin() + offs[5]);
     std::copy(P->splits.begin(), P->splits.end(), h.begin() + offs[6]);
+    std::copy(P->chunk_ptr.begin(), P->chunk_ptr.end(), h.begin() + offs[7]);
     void* buf = nullptr;
     if (cudaMalloc(&buf, total * sizeof(int32_t)) != cudaSuccess) {
         cudaGetLastError();
@@ -142,6 +147,7 @@ int ensure_device(tree_attn_plan_s* P, DevicePlan** out) {
     D.kv_minsub = b + offs[4];
     D.bwd_items = b + offs[5];
     D.splits = b + offs[6];
+    D.chunk_ptr = b + offs[7];
     D.ready = true;
     *out = &D;
     return TREE_ATTN_OK;
@@ -185,6 +191,22 @@ WsLayout bwd_layout(const tree_attn_plan_s* P, int hq, int hkv, int d) {
     w.part = w.lse2 + up(Npad * hq * 4);
     w.total = w.part + up((size_t)P->n_slots * hkv * 2 * kBlock * d * 4);
     return w;
+}
+
+// Backward CTA order.  Item-major spreads the CTAs running at one time over
+// every kv-head's dQ rows of the current chunk; when those rows (chunk q-tiles
+// x 128 x hq x d fp32) are larger than about 3/4 of the 129 MB L2, the
+// reduce-adds miss, and the head-major order (one kv-head group's rows at a
+// time) keeps them in L2.  Measured on the long shared context (chunk 48,
+// 64 q-heads: 201 MB of rows): 1,113 vs 1,070 TFLOP/s; on the GRPO star
+// (chunk 24, 32 q-heads: 50 MB) item-major is the faster one.
+constexpr size_t kHeadMajorRowBytes = 96ull << 20;
+
+void set_cta_order(BwdParams& p, const tree_attn_plan_s* P, const int32_t* chunk_ptr, int hq, int d) {
+    p.chunk_ptr = chunk_ptr;
+    p.n_chunks = (int32_t)P->chunk_ptr.size() - 1;
+    const size_t rows = (size_t)P->chunk * kBlock * hq * d * 4;
+    p.head_major = (rows > kHeadMajorRowBytes && p.n_chunks > 0) ? 1 : 0;
 }
 
 }  // namespace
@@ -297,6 +319,8 @@ int tree_attn_fwd(tree_attn_plan_t P, const void* q, const void* k, const void* 
     p.hq = hq;
     p.group = group;
     p.scale_log2 = softmax_scale * 1.4426950408889634f;
+    p.T = P->T;
+    p.n_ent = (int64_t)P->qt_kv.size();
     int dev = 0;
     cudaGetDevice(&dev);
     if ((st = status_ptr(dev, &p.status))) return st;
@@ -357,6 +381,7 @@ int tree_attn_bwd_stages(tree_attn_plan_t P, const void* q, const void* k, const
 
     BwdParams p;
     p.items = D->bwd_items;
+    set_cta_order(p, P, D->chunk_ptr, hq, d);
     p.subend = D->subend;
     p.kv_minsub = D->kv_minsub;
     p.delta = pre.delta;
@@ -372,6 +397,9 @@ int tree_attn_bwd_stages(tree_attn_plan_t P, const void* q, const void* k, const
     p.group = hq / hkv;
     p.scale = softmax_scale;
     p.scale_log2 = softmax_scale * 1.4426950408889634f;
+    p.T = P->T;
+    p.n_items = (int32_t)(P->bwd_items.size() / 4);
+    p.n_slots = P->n_slots;
     int dev = 0;
     cudaGetDevice(&dev);
     if ((st = status_ptr(dev, &p.status))) return st;
@@ -394,6 +422,9 @@ int tree_attn_bwd_stages(tree_attn_plan_t P, const void* q, const void* k, const
     post.hkv = hkv;
     post.d = d;
     post.n_splits = (int32_t)(P->splits.size() / 4);
+    post.T = P->T;
+    post.n_slots = P->n_slots;
+    post.status = p.status;
     if (stages & TREE_ATTN_BWD_POST) e = launch_bwd_post(post, s);
     return e == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
 }
@@ -450,9 +481,10 @@ int tree_attn_bwd_noalloc(tree_attn_plan_t P, const void* q, const void* k, cons
     const int64_t n_ent = (int64_t)P->qt_kv.size();
     const int64_t n_items = (int64_t)P->bwd_items.size() / 4;
     const int64_t n_splits = (int64_t)P->splits.size() / 4;
-    const int64_t sizes[5] = {T * kBlock, T, 4 * n_items, 4 * std::max<int64_t>(n_splits, 1), 0};
-    int64_t offs[5], words = 0;
-    for (int i = 0; i < 5; ++i) {
+    const int64_t sizes[6] = {T * kBlock, T, 4 * n_items, 4 * std::max<int64_t>(n_splits, 1),
+                              (int64_t)P->chunk_ptr.size(), 0};
+    int64_t offs[6], words = 0;
+    for (int i = 0; i < 6; ++i) {
         offs[i] = words;
         words += (sizes[i] + 63) / 64 * 64;
     }
@@ -472,6 +504,7 @@ int tree_attn_bwd_noalloc(tree_attn_plan_t P, const void* q, const void* k, cons
     std::copy(P->kv_minsub.begin(), P->kv_minsub.end(), h.begin() + offs[1]);
     std::copy(P->bwd_items.begin(), P->bwd_items.end(), h.begin() + offs[2]);
     std::copy(P->splits.begin(), P->splits.end(), h.begin() + offs[3]);
+    std::copy(P->chunk_ptr.begin(), P->chunk_ptr.end(), h.begin() + offs[4]);
     // pageable source: the copy is staged before the call returns
     if (cudaMemcpyAsync(scratch, h.data(), table_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
         return TREE_ATTN_ERR_CUDA;
@@ -500,6 +533,7 @@ int tree_attn_bwd_noalloc(tree_attn_plan_t P, const void* q, const void* k, cons
 
     BwdParams p;
     p.items = tab + offs[2];
+    set_cta_order(p, P, tab + offs[4], hq, d);
     p.subend = tab + offs[0];
     p.kv_minsub = tab + offs[1];
     p.delta = pre.delta;
@@ -515,6 +549,9 @@ int tree_attn_bwd_noalloc(tree_attn_plan_t P, const void* q, const void* k, cons
     p.group = hq / hkv;
     p.scale = softmax_scale;
     p.scale_log2 = softmax_scale * 1.4426950408889634f;
+    p.T = P->T;
+    p.n_items = (int32_t)(P->bwd_items.size() / 4);
+    p.n_slots = P->n_slots;
     p.status = status;
     if ((st = launch_main(d, tq, tk, tv, tdo, tdq, p, (int)(n_items * hkv), s)))
         return st;
@@ -531,6 +568,9 @@ int tree_attn_bwd_noalloc(tree_attn_plan_t P, const void* q, const void* k, cons
     post.hkv = hkv;
     post.d = d;
     post.n_splits = (int32_t)n_splits;
+    post.T = P->T;
+    post.n_slots = P->n_slots;
+    post.status = status;
     return launch_bwd_post(post, s) == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
 }
 
@@ -544,6 +584,22 @@ int tree_attn_selftest_wait_timeout(int32_t limit_ms, void* stream) {
     int* status = nullptr;
     if ((st = status_ptr(dev, &status))) return st;
     treeattn::launch_wait_selftest(status, (uint64_t)limit_ms * 1000000ull, static_cast<cudaStream_t>(stream));
+    return cudaGetLastError() == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
+}
+
+int tree_attn_debug_checks(void) { return treeattn::kDebugChecks ? 1 : 0; }
+
+int tree_attn_selftest_bounds(void* stream) {
+    if (!treeattn::kDebugChecks) return TREE_ATTN_ERR_UNSUPPORTED;
+    int dev;
+    int st = current_device(&dev);
+    if (st) return st;
+    int* status = nullptr;
+    if ((st = status_ptr(dev, &status))) return st;
+    // the word the kernel would write if its check passed
+    int* out = nullptr;
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&out), g_selftest_word) != cudaSuccess) return TREE_ATTN_ERR_CUDA;
+    treeattn::launch_bounds_selftest(status, out, static_cast<cudaStream_t>(stream));
     return cudaGetLastError() == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
 }
 
@@ -589,8 +645,11 @@ const char* tree_attn_strerror(int s) {
                    "(see tree_attn_noalloc_scratch_bytes)";
         case TREE_ATTN_ERR_DEVICE_TIMEOUT: return "a bounded device wait ran out";
         case TREE_ATTN_ERR_INVALID_DECAY: return "linear-attention decay outside (0, 1]";
+        case TREE_ATTN_ERR_DEVICE_BOUNDS: return "a debug bounds check failed";
         default:
-            if (s <= TREE_ATTN_ERR_DEVICE_TIMEOUT - 1000) return "a bounded device wait ran out";
+            // status words with a site: code - 1000 * site
+            if (s <= -1000 && (-s) % 1000 == -TREE_ATTN_ERR_DEVICE_TIMEOUT) return "a bounded device wait ran out";
+            if (s <= -1000 && (-s) % 1000 == -TREE_ATTN_ERR_DEVICE_BOUNDS) return "a debug bounds check failed";
             return "unknown status";
     }
 }

@@ -81,6 +81,10 @@ __global__ void __launch_bounds__(256) dkv_reduce_kernel(const BwdPostParams p) 
     const int si = (rest >> 1) / p.hkv;
     const int4 sp = reinterpret_cast<const int4*>(p.splits)[si];
     const int c = sp.x, base = sp.y, nslot = sp.z;
+    // debug builds: the split's kv-tile and slot range must lie inside the plan
+    if (!(ta_ok(p.status, 401, c, 0, p.T) && ta_ok(p.status, 402, base, 0, p.n_slots) &&
+          ta_ok(p.status, 403, (long long)base + nslot - 1, base, p.n_slots)))
+        return;
     const int per_tile = 128 * p.d;
     const int per_group = per_tile / kDkvRowGroups;
     uint16_t* out = which == 0 ? p.dk : p.dv;
@@ -136,10 +140,21 @@ __global__ void wait_selftest_kernel(int* status, uint64_t limit_ns) {
     report_status(status, -10 - 1000 * 99);
 }
 
+// One thread checks an index that lies outside its range on purpose: in debug
+// builds the check records site 98 and the (never made) access is skipped.
+__global__ void bounds_selftest_kernel(int* status, int* out) {
+    const int index = 5, size = 4;
+    if (ta_ok(status, 98, index, 0, size)) *out = index;
+}
+
 }  // namespace
 
 void launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t stream) {
     wait_selftest_kernel<<<1, 1, 0, stream>>>(status, limit_ns);
+}
+
+void launch_bounds_selftest(int* status, int* out, cudaStream_t stream) {
+    bounds_selftest_kernel<<<1, 1, 0, stream>>>(status, out);
 }
 
 cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t stream) {

@@ -135,10 +135,17 @@ __global__ void __launch_bounds__(FsCfg<NCW>::NWARPS * 32, 1)
         if (threadIdx.x == 0) report_status(p.status, -5);
         return;
     }
-    const int item = blockIdx.x / p.hkv;
-    const int hk = blockIdx.x % p.hkv;
+    int item, hk;
+    bwd_cta_work(p, blockIdx.x, item, hk);
+    if (item < 0) return;   // debug builds: the CTA index maps to no item
     const int4 it = reinterpret_cast<const int4*>(p.items)[item];
     const int c = it.x, t0 = it.y, t1 = it.z, slot = it.w;
+    // debug builds: the item's kv-tile, q-range, slot and kv-head must lie inside
+    // the plan's tables (a uniform return, before any barrier or TMEM is set up)
+    if (!(ta_ok(p.status, 211, c, 0, p.T) && ta_ok(p.status, 212, t0, c, p.T) &&
+          ta_ok(p.status, 213, t1, t0 + 1, (long long)p.T + 1) && ta_ok(p.status, 214, slot, -1, p.n_slots) &&
+          ta_ok(p.status, 215, hk, 0, p.hkv)))
+        return;
     const int G = p.group;
     const int nsteps = (t1 - t0) * G;
 
@@ -206,7 +213,8 @@ __global__ void __launch_bounds__(FsCfg<NCW>::NWARPS * 32, 1)
                 if (n >= 2) ok = mbar_wait(bar(C::B_LEMPTY + 8 * ls), ((n >> 1) - 1) & 1, p.status, 62);
                 if (!ok) break;
                 mbar_expect_tx(bar(C::B_LFULL + 8 * ls), 1024);
-                const size_t off = (size_t)h * p.Npad + (size_t)t * 128;
+                const size_t off = (size_t)ta_clamp(p.status, 216, (long long)h * p.Npad + (long long)t * 128, 0,
+                                                    (long long)p.hq * p.Npad - 127);
                 bulk_load(sb + C::LSD + ls * 1024, p.lse2 + off, 512, bar(C::B_LFULL + 8 * ls));
                 bulk_load(sb + C::LSD + ls * 1024 + 512, p.delta + off, 512, bar(C::B_LFULL + 8 * ls));
                 // dO(n), once dV(n-1) has read dO(n-1)
@@ -377,7 +385,7 @@ __global__ void __launch_bounds__(FsCfg<NCW>::NWARPS * 32, 1)
         const int r = (quarter << 5) + lane;           // TMEM lane = this thread's key
         const uint32_t lane_base = tmem + ((uint32_t)(quarter << 5) << 16);
         const int j = c * 128 + r;
-        const int sub_j = p.subend[j];                 // 0 past N
+        const int sub_j = p.subend[ta_clamp(p.status, 217, j, 0, (long long)p.T * 128)];   // 0 past N
         const float sl2 = p.scale_log2;
         const uint32_t dsa = sb + C::OFF_DST;
         bool ok = true;

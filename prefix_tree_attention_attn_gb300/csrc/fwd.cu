@@ -98,8 +98,14 @@ __global__ void __launch_bounds__(FwdCfg<D, NS, PER_SM>::NWARPS * 32, PER_SM)
     const int h0 = (blockIdx.x % n_hg) * NS;
     const int hk = h0 / p.group;
     const int q0 = t * 128;
+    // debug builds: the q-tile, its kv-tile list and the heads must lie inside
+    // the plan's tables (a uniform return, before any barrier or TMEM is set up)
+    if (!(ta_ok(p.status, 101, t, 0, p.T) && ta_ok(p.status, 102, h0 + NS - 1, 0, p.hq)))
+        return;
     const int e0 = p.qt_ptr[t];
     const int n_kv = p.qt_ptr[t + 1] - e0;  // >= 1: the diagonal block is never empty
+    if (!(ta_ok(p.status, 103, e0, 0, p.n_ent) && ta_ok(p.status, 104, (long long)e0 + n_kv - 1, e0, p.n_ent)))
+        return;
 
     const uint32_t b_qfull = sb + C::B_QFULL;
     auto b_kvfull = [&](int s) { return sb + C::B_KVFULL + 8 * s; };
@@ -140,7 +146,8 @@ __global__ void __launch_bounds__(FwdCfg<D, NS, PER_SM>::NWARPS * 32, PER_SM)
                     tma_load_3d(sb + C::OFF_Q + s * C::TILE + blk * 16384, &tm_q, blk * 64, h0 + s, q0, b_qfull);
             bool ok = true;
             for (int j = 0; j < n_kv && ok; ++j) {
-                const int c = p.qt_ent[e0 + j] >> 1;
+                // debug builds: an out-of-range kv-tile is reported and kv-tile 0 loaded instead
+                const int c = (int)ta_clamp(p.status, 105, p.qt_ent[e0 + j] >> 1, 0, p.T);
                 for (int kv = 0; kv < 2 && ok; ++kv) {
                     const int pos = 2 * j + kv, slot = pos % C::NSLOT, use = pos / C::NSLOT;
                     if (use > 0) ok = mbar_wait(b_kvempty(slot), (use - 1) & 1, p.status, 1);
@@ -230,11 +237,13 @@ __global__ void __launch_bounds__(FwdCfg<D, NS, PER_SM>::NWARPS * 32, PER_SM)
         // The tile list, this row's subtree end of each partial tile's keys and the
         // tile's minimum subtree end are loaded a tile ahead (the list entry two
         // ahead), so no global-memory latency sits on a tile's critical path.
+        // (debug builds: subtree ends and minima read at clamped kv-tiles)
+        auto kv_of = [&](int ent) { return (int)ta_clamp(p.status, 106, ent >> 1, 0, p.T); };
         int ent_next = p.qt_ent[e0];
         int sub_next = 0, min_next = 0;
         if (ent_next & 1) {
-            sub_next = p.subend[(ent_next >> 1) * 128 + r];
-            min_next = p.kv_minsub[ent_next >> 1];
+            sub_next = p.subend[kv_of(ent_next) * 128 + r];
+            min_next = p.kv_minsub[kv_of(ent_next)];
         }
         int ent_after = n_kv > 1 ? p.qt_ent[e0 + 1] : 0;
         for (int j = 0; j < n_kv; ++j) {
@@ -244,8 +253,8 @@ __global__ void __launch_bounds__(FwdCfg<D, NS, PER_SM>::NWARPS * 32, PER_SM)
             const int my_sub = sub_next, kv_min = min_next;
             ent_next = ent_after;
             if (j + 1 < n_kv && (ent_next & 1)) {
-                sub_next = p.subend[(ent_next >> 1) * 128 + r];
-                min_next = p.kv_minsub[ent_next >> 1];
+                sub_next = p.subend[kv_of(ent_next) * 128 + r];
+                min_next = p.kv_minsub[kv_of(ent_next)];
             }
             if (j + 2 < n_kv) ent_after = p.qt_ent[e0 + j + 2];
             // After a failed wait the loop keeps running (work skipped) so that every

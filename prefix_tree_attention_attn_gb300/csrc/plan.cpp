@@ -270,6 +270,11 @@ int build_plan(const int32_t* parent, const int32_t* seg_len, int32_t n, const t
         P->bwd_items.resize(items.size());
         for (int32_t i = 0; i < n_items; ++i)
             for (int f = 0; f < 4; ++f) P->bwd_items[4 * i + f] = items[4 * idx[i] + f];
+        // CSR of the items of each chunk (chunks with no item are empty ranges)
+        const int32_t n_chunks = (T + S - 1) / S;
+        P->chunk_ptr.assign(n_chunks + 1, 0);
+        for (int32_t i = 0; i < n_items; ++i) P->chunk_ptr[chunk_of[idx[i]] + 1]++;
+        for (int32_t k = 0; k < n_chunks; ++k) P->chunk_ptr[k + 1] += P->chunk_ptr[k];
     } catch (const std::bad_alloc&) {
         delete P;
         return TREE_ATTN_ERR_OUT_OF_MEMORY;

@@ -24,6 +24,7 @@ struct DevicePlan {
     int32_t* kv_minsub = nullptr;  // [T]
     int32_t* bwd_items = nullptr;  // [4*items]
     int32_t* splits = nullptr;     // [4*splits] {kv-tile, first slot, n slots, 0}
+    int32_t* chunk_ptr = nullptr;  // [n_chunks+1] first backward item of each q-range chunk
     bool ready = false;
     // trajectory tables of the loss-boundary calls (uploaded on their first use)
     void* traj_base = nullptr;
@@ -76,6 +77,7 @@ struct Plan {
     std::vector<int32_t> fwd_order;
     std::vector<int32_t> bwd_items;   // 4 per item
     std::vector<int32_t> splits;      // 4 per split kv-tile
+    std::vector<int32_t> chunk_ptr;   // items of chunk k: [chunk_ptr[k], chunk_ptr[k+1])
     int64_t n_slots = 0;
     std::vector<int32_t> parent, seg_len;   // the tree as given
     TrajInfo traj;                          // guarded by mu

@@ -23,6 +23,36 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 // A wait that ran out is stored as -10 - 1000 * where.
 __device__ __forceinline__ void report_status(int* status, int code) { atomicCAS(status, 0, code); }
 
+// ---- debug bounds checks -------------------------------------------------------
+// Builds with -DTREE_ATTN_DEBUG check the indices that come from the plan's
+// tables and the tree's shape (work items, kv-tile lists, subtree ends, partial
+// dK/dV slots, LSE / Delta rows, head numbers) before they address global
+// memory.  A failed check records TREE_ATTN_ERR_DEVICE_BOUNDS - 1000 * site in
+// the status word (the first error wins) and the access is skipped (ta_ok) or
+// made at a clamped in-range index (ta_clamp), so nothing is read or written out
+// of bounds and no wait is left hanging.  Other builds compile the checks away.
+#ifdef TREE_ATTN_DEBUG
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+constexpr int kErrDeviceBounds = -13;   // TREE_ATTN_ERR_DEVICE_BOUNDS
+
+// lo <= v < hi, or report the site and return false
+__device__ __forceinline__ bool ta_ok(int* status, int site, long long v, long long lo, long long hi) {
+    if constexpr (kDebugChecks) {
+        if (v < lo || v >= hi) {
+            atomicCAS(status, 0, kErrDeviceBounds - 1000 * site);
+            return false;
+        }
+    }
+    return true;
+}
+// v if lo <= v < hi, else lo after reporting the site
+__device__ __forceinline__ long long ta_clamp(int* status, int site, long long v, long long lo, long long hi) {
+    return ta_ok(status, site, v, lo, hi) ? v : lo;
+}
+
 // ---- mbarrier --------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

@@ -31,7 +31,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_status_codes_named(lib):
     text = open(HEADER).read()
     codes = {int(v) for v in re.findall(r"#define TREE_ATTN_(?:OK|ERR_[A-Z_]+)\s+(-?\d+)", text)}
-    assert codes == set(range(-12, 1))
+    assert codes == set(range(-13, 1))
     for code in codes:
         s = lib.tree_attn_strerror(code).decode()
         assert s and s != "unknown status"
@@ -170,3 +170,15 @@ def test_tensors_must_match_the_plan_before_any_launch(lib):
             tree_linear_fwd(p, bad_q, kk, vv, dec, 1.0, o=t(n_q, hq), workspace=good_q)
         with pytest.raises(ValueError):
             tree_linear_bwd(p, bad_q, kk, vv, t(n_q, hq), dec, 1.0, workspace=good_q, **outs)
+
+
+def test_debug_build_flags(lib):
+    """The release library carries no bounds checks (its self-test refuses);
+    the twin built with -DTREE_ATTN_DEBUG says it has them."""
+    from prefix_tree_attention_attn_gb300 import build as _build
+    assert lib.tree_attn_debug_checks() == 0
+    assert lib.tree_attn_selftest_bounds(None) == -4
+    dl = B.load(_build.build_library(debug=True))
+    assert dl.tree_attn_debug_checks() == 1
+    assert lib.tree_attn_strerror(-13 - 1000 * 211).decode() == "a debug bounds check failed"
+    assert lib.tree_attn_strerror(-10 - 1000 * 67).decode() == "a bounded device wait ran out"

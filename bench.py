@@ -578,9 +578,9 @@ def run_ours(args):
         h2d = sum(t_.numel() * t_.element_size() for t_ in pin.values())
         d2h = sum(t_.numel() * t_.element_size() for t_ in outs.values())
         # a bounded number of end-to-end steps: about 20 s at most
-        e2e_steps = max(2, min(args.steps, 20, int(20e3 / (1.5 * summ["ms_per_step"] + 1.0))))
-        e2e_warm = 1 if long_step else max(3, args.warmup)
-        side = torch.cuda.Stream(device=dev)        # copies that can overlap compute
+        e2e_steps = max(3, min(args.steps, 20, int(20e3 / (1.5 * summ["ms_per_step"] + 1.0))))
+        e2e_warm = 2 if long_step else max(3, args.warmup)
+        side = torch.cuda.Stream(device=dev)        # the dO upload overlaps the forward
 
         def e2e_step():
             main = torch.cuda.current_stream(dev)
@@ -591,15 +591,12 @@ def run_ours(args):
                 dod = pin["do"].to(dev, non_blocking=True)   # arrives during the forward
             p2 = TA.TreePlan(tree.parent, tree.seg_len)      # a new tree each step: plan on the host
             oo, ll = TA.tree_attn_fwd(p2, qd, kd, vd, scale)
-            fwd_done = torch.cuda.Event()
-            fwd_done.record(main)
             main.wait_stream(side)
             a, b, c = TA.tree_attn_bwd(p2, qd, kd, vd, oo, ll, dod, scale)
-            with torch.cuda.stream(side):                    # O and LSE leave during the backward
-                side.wait_event(fwd_done)
-                outs["o"].copy_(oo, non_blocking=True)
-                outs["lse"].copy_(ll, non_blocking=True)
-            for nm, src in (("dq", a), ("dk", b), ("dv", c)):
+            # the outputs leave after the backward: copies that run during it slow it
+            # down by more than they hide (long shared context: 1.88 s per step this
+            # way, 1.89-1.94 s with O and LSE leaving during the backward)
+            for nm, src in (("o", oo), ("lse", ll), ("dq", a), ("dk", b), ("dv", c)):
                 outs[nm].copy_(src, non_blocking=True)
             torch.cuda.synchronize(dev)      # the step's results are on the host
             p2.close()
@@ -614,8 +611,8 @@ def run_ours(args):
         e2e = {"value": flops_step * world / e2e_s / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3, "steps": e2e_steps,
                "includes": "host plan build + device upload, H2D of q/k/v/dO from pinned memory, fwd+bwd, "
-                           "D2H of o/lse/dq/dk/dv; dO arrives during the forward and O/LSE leave during the "
-                           "backward (side stream)"}
+                           "D2H of o/lse/dq/dk/dv after the backward; dO arrives during the forward (side "
+                           "stream)"}
         del pin, outs
         torch.cuda.empty_cache()
 

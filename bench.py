@@ -426,11 +426,15 @@ def device_inputs(WX, name, n_tokens, dev):
     return heads, rec, {n: t.to(dev) for n, t in x.items()}
 
 
-def timed_hot_path(torch, TA, plan, x, heads, scale, steps, warmup, flush, around=None):
+def timed_hot_path(torch, TA, plan, x, heads, scale, steps, warmup, flush, around=None, graph_out=None):
     """Warm up, then time ``steps`` steps (forward, backward pre / main / post)
     with CUDA events on the launching stream, L2 flushed (untimed) before
     each.  ``around`` = (enter, leave) callables wrapped round the timed
-    region.  Returns per-step [fwd, pre, main, post] milliseconds."""
+    region.  Returns per-step [fwd, pre, main, post] milliseconds.  With
+    ``graph_out`` (a dict), the same step is also captured once in a CUDA graph
+    (the launch-bound small trees: five launches per step become one) and its
+    replays timed the same way; the per-step milliseconds land in
+    graph_out["ms"]."""
     hq, hkv, d = heads.hq, heads.hkv, heads.d
     N = plan.n_tokens
     q, k, v, do = x["q"], x["k"], x["v"], x["do"]
@@ -470,8 +474,26 @@ def timed_hot_path(torch, TA, plan, x, heads, scale, steps, warmup, flush, aroun
     status = TA.device_status()
     if status != 0:
         raise RuntimeError(f"device status {status}")
+    per = [[e[i].elapsed_time(e[i + 1]) for i in range(4)] for e in evs]
+    if graph_out is not None:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        for _ in range(3):
+            g.replay()
+        ge = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        for kk in range(steps):
+            flush.fill_(kk & 0xff)
+            ge[kk][0].record()
+            g.replay()
+            ge[kk][1].record()
+        torch.cuda.synchronize()
+        if TA.device_status() != 0:
+            raise RuntimeError("device status non-zero after graph replays")
+        graph_out["ms"] = [a.elapsed_time(b) for a, b in ge]
+        del g
     del o, lse, dq, dk, dv, ws
-    return [[e[i].elapsed_time(e[i + 1]) for i in range(4)] for e in evs]
+    return per
 
 
 def stage_summary(per, f_fwd, f_bwd):
@@ -670,8 +692,12 @@ def run_ours(args):
             hw, rw, xw = device_inputs(WX, wn, tw.n_tokens, dev)
             pw = TA.TreePlan(tw.parent, tw.seg_len)
             ff, fb = useful_flops(pw.n_pairs, hw.hq, hw.d)
-            pr = timed_hot_path(torch, TA, pw, xw, hw, rw.scale, min(args.steps, 20), 3, flush)
+            gr = {}
+            pr = timed_hot_path(torch, TA, pw, xw, hw, rw.scale, min(args.steps, 20), 3, flush, graph_out=gr)
             sw = stage_summary(pr, ff, fb)
+            gms = statistics.mean(gr["ms"])
+            sw["graph"] = {"ms_per_step": gms, "tflops": (ff + fb) / (gms / 1e3) / 1e12,
+                           "what": "the same five launches captured once in a CUDA graph and replayed"}
             sw.update({"name": wn, "workload": DESCRIPTIONS[wn], "n_tokens": pw.n_tokens, "pairs": pw.n_pairs,
                        "hq": hw.hq, "hkv": hw.hkv, "d": hw.d, "steps": len(pr),
                        "pct_peak": 100.0 * sw["tflops"] / peak_burst, "peak": f"{peak_src} bf16 burst"})

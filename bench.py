@@ -627,11 +627,15 @@ def run_ours(args):
             e2e_step()
         barrier()
         t0 = time.perf_counter()
+        e2e_each = []
         for _ in range(e2e_steps):
+            t1 = time.perf_counter()
             e2e_step()
+            e2e_each.append(time.perf_counter() - t1)
         e2e_s = (time.perf_counter() - t0) / e2e_steps
         e2e = {"value": flops_step * world / e2e_s / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3, "steps": e2e_steps,
+               "ms_each": [round(t_ * 1e3, 2) for t_ in e2e_each],
                "includes": "host plan build + device upload, H2D of q/k/v/dO from pinned memory, fwd+bwd, "
                            "D2H of o/lse/dq/dk/dv after the backward; dO arrives during the forward (side "
                            "stream)"}

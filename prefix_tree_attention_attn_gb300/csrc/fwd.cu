@@ -291,25 +291,18 @@ __global__ void __launch_bounds__(FwdCfg<D, NS, PER_SM>::NWARPS * 32, PER_SM)
                     }
                 }
             };
-            // The next 32 columns are loaded while this 32 are processed (two
-            // register buffers), so a TMEM load's latency is exposed once per pass
-            // instead of four times.  A masked write-back lands on columns already
-            // read, never on the ones in flight.
             float mraw = -INFINITY;
-            float va[32], vb[32];
-            tmem_ld32(tS, va);
-            tmem_wait_ld();
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
-                float(&v)[32] = (cc & 1) ? vb : va;
-                if (cc < 3) tmem_ld32(tS + (cc + 1) * 32, (cc & 1) ? va : vb);
+                float v[32];
+                tmem_ld32(tS + cc * 32, v);
+                tmem_wait_ld();
                 if (need_mask) {
                     mask(v, cc);
                     tmem_st32(tS + cc * 32, v);
                 }
 #pragma unroll
                 for (int u = 0; u < 32; u += 2) mraw = fmax3(mraw, v[u], v[u + 1]);
-                if (cc < 3) tmem_wait_ld();
             }
             if (need_mask) tmem_wait_st();
             const float mx = mraw * sl2;   // softmax_scale > 0, so the maximum commutes with it
@@ -340,13 +333,11 @@ __global__ void __launch_bounds__(FwdCfg<D, NS, PER_SM>::NWARPS * 32, PER_SM)
             // columns); the per-lane results equal the scalar fmaf / add.
             const uint64_t scale2 = f32x2(sl2, sl2), negm2 = f32x2(-m_use, -m_use);
             uint64_t lsum2 = f32x2(0.f, 0.f);
-            // (pass 1's masked stores are complete: see the wait above)
-            tmem_ld32(tS, va);
-            tmem_wait_ld();
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
-                float(&v)[32] = (cc & 1) ? vb : va;
-                if (cc < 3) tmem_ld32(tS + (cc + 1) * 32, (cc & 1) ? va : vb);
+                float v[32];
+                tmem_ld32(tS + cc * 32, v);
+                tmem_wait_ld();
                 uint32_t pw[16];
 #pragma unroll
                 for (int h = 0; h < 16; ++h) {
@@ -357,7 +348,6 @@ __global__ void __launch_bounds__(FwdCfg<D, NS, PER_SM>::NWARPS * 32, PER_SM)
                     pw[h] = pack_bf16x2(a, b);
                 }
                 tmem_st16(tS + cc * 16, pw);
-                if (cc < 3) tmem_wait_ld();
             }
             float lsa, lsb;
             f32x2_split(lsum2, lsa, lsb);

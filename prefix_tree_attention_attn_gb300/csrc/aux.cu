@@ -27,6 +27,8 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
 // dO rows, which the backward's first work items touch, are then the ones
 // written or read most recently and still in L2.
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
+    grid_dep_wait();   // O and LSE come from the forward
+    grid_dep_launch();
     const int lanes = p.d >> 3;                                   // 16 (d = 128) or 8 (d = 64)
     const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t total = (int64_t)p.Npad * p.hq;
@@ -61,6 +63,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
 // dQ: 4 elements per thread.
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ src, uint16_t* __restrict__ dst,
                                                          int64_t n4) {
+    grid_dep_wait();   // the accumulator is complete once the main pass has finished
+    grid_dep_launch();
     const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (k >= n4) return;
     const float4 v = reinterpret_cast<const float4*>(src)[k];
@@ -74,6 +78,8 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
 // consecutive elements of the group's 16 x d slice of the 128 x d tile.
 constexpr int kDkvRowGroups = 8;
 __global__ void __launch_bounds__(256) dkv_reduce_kernel(const BwdPostParams p) {
+    grid_dep_wait();   // the partial slots come from the main pass (the dQ conversion runs between)
+    grid_dep_launch();
     const int rg = blockIdx.x % kDkvRowGroups;
     const int rest = blockIdx.x / kDkvRowGroups;
     const int which = rest & 1;
@@ -161,21 +167,18 @@ cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t stream) {
     const int64_t threads = (int64_t)p.Npad * p.hq * (p.d / 8);
     const int64_t blocks = (threads + 255) / 256;
     if (blocks > INT32_MAX) return cudaErrorInvalidValue;
-    bwd_pre_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(bwd_pre_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, p);
 }
 
 cudaError_t launch_bwd_post(const BwdPostParams& p, cudaStream_t stream) {
     const int64_t n4 = (int64_t)p.N * p.hq * p.d / 4;
     const int64_t blocks = (n4 + 255) / 256;
     if (blocks > INT32_MAX) return cudaErrorInvalidValue;
-    if (blocks > 0) dq_convert_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p.dq_acc, p.dq, n4);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = cudaSuccess;
+    if (blocks > 0) e = launch_pdl(dq_convert_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, p.dq_acc, p.dq, n4);
     if (e != cudaSuccess) return e;
-    if (p.n_splits > 0) {
-        dkv_reduce_kernel<<<p.n_splits * p.hkv * 2 * kDkvRowGroups, 256, 0, stream>>>(p);
-        e = cudaGetLastError();
-    }
+    if (p.n_splits > 0)
+        e = launch_pdl(dkv_reduce_kernel, dim3(p.n_splits * p.hkv * 2 * kDkvRowGroups), dim3(256), 0, stream, p);
     return e;
 }
 

@@ -124,6 +124,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::NWARPS * 32, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::HOLDER);
+    // Delta, LSE and the zeroed dQ accumulator come from the pre kernel just before
+    grid_dep_wait();
+    grid_dep_launch();
 
     // ring position of step n's Q (w = 0) or dO (w = 1)
     auto ring_pos = [](int n, int w) { return 2 * n + w; };
@@ -456,8 +459,7 @@ cudaError_t launch_cfg(const CUtensorMap* tq, const CUtensorMap* tk, const CUten
     auto kern = bwd_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES);
     if (e != cudaSuccess) return e;
-    kern<<<grid, C::NWARPS * 32, C::BYTES, stream>>>(*tq, *tk, *tv, *tdo, *tdq, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(C::NWARPS * 32), C::BYTES, stream, *tq, *tk, *tv, *tdo, *tdq, p);
 }
 
 }  // namespace

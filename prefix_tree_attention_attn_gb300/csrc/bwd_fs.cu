@@ -175,6 +175,9 @@ __global__ void __launch_bounds__(FsCfg<NCW>::NWARPS * 32, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::HOLDER);
+    // Delta, LSE and the zeroed dQ accumulator come from the pre kernel just before
+    grid_dep_wait();
+    grid_dep_launch();
     if (threadIdx.x == 0) BWD_TRACE(20, 0);
 
     if (warp == C::PRODUCER) {
@@ -532,8 +535,7 @@ cudaError_t launch_fs(const CUtensorMap* tq, const CUtensorMap* tk, const CUtens
     auto kern = bwd_fs_kernel<NCW>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES);
     if (e != cudaSuccess) return e;
-    kern<<<grid, C::NWARPS * 32, C::BYTES, stream>>>(*tq, *tk, *tv, *tdo, *tdq, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(C::NWARPS * 32), C::BYTES, stream, *tq, *tk, *tv, *tdo, *tdq, p);
 }
 
 }  // namespace

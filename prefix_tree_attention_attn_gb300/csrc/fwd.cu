@@ -134,6 +134,9 @@ __global__ void __launch_bounds__(FwdCfg<D, NS, PER_SM>::NWARPS * 32, PER_SM)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::HOLDER);
+    // Q, K, V may come from the previous kernel, and O / LSE may still be read by it
+    grid_dep_wait();
+    grid_dep_launch();
 
     if (warp == C::PRODUCER) {
         if (lane == 0) {
@@ -404,8 +407,7 @@ cudaError_t launch_cfg(const CUtensorMap* tq, const CUtensorMap* tk, const CUten
     auto kern = fwd_kernel<D, NS, PER_SM>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES);
     if (e != cudaSuccess) return e;
-    kern<<<grid, C::NWARPS * 32, C::BYTES, stream>>>(*tq, *tk, *tv, *to, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(C::NWARPS * 32), C::BYTES, stream, *tq, *tk, *tv, *to, p);
 }
 
 }  // namespace

@@ -97,6 +97,24 @@ __device__ __forceinline__ void bwd_cta_work(const BwdParams& p, int b, int& ite
     item = base + r % n;
 }
 
+// Launch with programmatic stream serialization (see grid_dep_wait in ptx.cuh):
+// the kernel may begin while the previous kernel on the stream finishes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Launchers return cudaSuccess or the launch error.
 // nstream q-heads per CTA; per_sm = 2 (only with nstream = 1): the two-CTAs-per-SM shape
 cudaError_t launch_fwd(int d, int nstream, int per_sm, const CUtensorMap* tq, const CUtensorMap* tk,

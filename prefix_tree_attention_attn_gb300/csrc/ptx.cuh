@@ -53,6 +53,18 @@ __device__ __forceinline__ long long ta_clamp(int* status, int site, long long v
     return ta_ok(status, site, v, lo, hi) ? v : lo;
 }
 
+// ---- programmatic dependent launch -------------------------------------------
+// The attention kernels are launched with programmatic stream serialization, so
+// a kernel's CTAs may start (barrier setup, TMEM allocation, reads of the plan's
+// tables, which only an earlier host copy writes) while the previous kernel on
+// the stream is still finishing.  grid_dep_wait() blocks until that kernel has
+// completed and its writes are visible: every kernel calls it before it reads
+// anything a previous kernel may have written and before it writes anything.
+// grid_dep_launch(), called after the wait, lets the next kernel start early in
+// turn (so at most two grids overlap).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---- mbarrier --------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

@@ -615,9 +615,10 @@ def run_ours(args):
             oo, ll = TA.tree_attn_fwd(p2, qd, kd, vd, scale)
             main.wait_stream(side)
             a, b, c = TA.tree_attn_bwd(p2, qd, kd, vd, oo, ll, dod, scale)
-            # the outputs leave after the backward: copies that run during it slow it
-            # down by more than they hide (long shared context: 1.88 s per step this
-            # way, 1.89-1.94 s with O and LSE leaving during the backward)
+            # The outputs leave after the backward.  Measured on one box, long shared
+            # context: 1.90-1.96 s per step this way; 1.93-1.98 s with O and LSE
+            # leaving during the backward (the copy slows it); 2.09-2.17 s with
+            # device buffers made once and reused.
             for nm, src in (("o", oo), ("lse", ll), ("dq", a), ("dk", b), ("dv", c)):
                 outs[nm].copy_(src, non_blocking=True)
             torch.cuda.synchronize(dev)      # the step's results are on the host

@@ -37,6 +37,16 @@
  *    and streams at once.  Its device copy is uploaded on the first fwd/bwd on
  *    each device (or by tree_attn_plan_upload); that first call allocates
  *    device memory and synchronises, so make it outside stream capture.
+ *    After it, tree_attn_fwd, tree_attn_bwd and tree_attn_bwd_stages allocate
+ *    nothing and do not synchronise, so a whole step can be captured in a CUDA
+ *    graph and replayed (what launch-bound small trees want).
+ *  - The attention kernels are launched with programmatic stream
+ *    serialization: each one's set-up may overlap the end of the kernel before
+ *    it on the stream, and waits (griddepcontrol.wait) for that kernel to
+ *    complete before it reads or writes any tensor; each one then allows the
+ *    next kernel to start early.  A caller's own kernel launched after ours
+ *    with the same attribute must likewise wait before it reads our outputs
+ *    (kernels launched without it simply run after ours, as usual).
  */
 #ifndef TREE_ATTN_H
 #define TREE_ATTN_H

@@ -44,8 +44,9 @@ DESCRIPTIONS = {
     "tiny_binary": "tiny binary tree 64 + 2x32 + 4x32 tokens; 2 heads, d=64",
     "long_context": "long shared context: 32768-token prefix + 64 chains of 1-3 log-U[1k,8k] segments; "
                     "64q/8kv heads, d=128",
-    "long_context_4b": "long shared context, first 4 of its 64 branches (58,232 tokens); 32q/4kv heads, d=128 "
-                       "(a few GB: the case profiler captures run on)",
+    "long_context_4b": "long shared context, first 4 of its 64 branches (58,232 tokens); 48q/6kv heads, d=128 "
+                       "(6 GB: the case profiler captures run on; the backward takes the long context's "
+                       "chunk and CTA order)",
 }
 
 
@@ -416,7 +417,7 @@ def workload_tree(WT, name):
 def device_inputs(WX, name, n_tokens, dev):
     """Seeded bf16 Q, K, V, dO of a workload on the device."""
     if name == "long_context_4b":
-        heads, rec = WX.HeadConfig(32, 4, 128), WX.VALUE_RECIPES["long_context"]
+        heads, rec = WX.HeadConfig(48, 6, 128), WX.VALUE_RECIPES["long_context"]
         return heads, rec, WX.draw_inputs(n_tokens, heads, rec, 1005, device=str(dev), chunk_rows=65536)
     heads, rec = WX.HEADS[base_name(name)], WX.VALUE_RECIPES[name]
     if name in DEVICE_DRAWN:

@@ -91,8 +91,9 @@ typedef struct {
                                  kernels run 128 only; other sizes (1..1024)
                                  are accepted for inspecting the plan.        */
     int32_t bwd_chunk_qtiles; /* max q-tiles per backward work item; 0 = auto:
-                                 24, doubled while the kv-tiles split over
-                                 several items would need more than
+                                 24 for fewer than 64 q-tiles, 48 for fewer
+                                 than 256, else 64; doubled while the kv-tiles
+                                 split over several items would need more than
                                  max(2048, 8 * n_qtiles) partial slots        */
 } tree_attn_plan_opts_t;
 

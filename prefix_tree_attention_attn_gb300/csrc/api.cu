@@ -194,13 +194,14 @@ WsLayout bwd_layout(const tree_attn_plan_s* P, int hq, int hkv, int d) {
 }
 
 // Backward CTA order.  Item-major spreads the CTAs running at one time over
-// every kv-head's dQ rows of the current chunk; when those rows (chunk q-tiles
-// x 128 x hq x d fp32) are larger than about 3/4 of the 129 MB L2, the
-// reduce-adds miss, and the head-major order (one kv-head group's rows at a
-// time) keeps them in L2.  Measured on the long shared context (chunk 48,
-// 64 q-heads: 201 MB of rows): 1,113 vs 1,070 TFLOP/s; on the GRPO star
-// (chunk 24, 32 q-heads: 50 MB) item-major is the faster one.
-constexpr size_t kHeadMajorRowBytes = 96ull << 20;
+// every kv-head's dQ rows (and Q / dO tiles) of the current chunk; head-major
+// runs one kv-head group at a time.  Measured backward main pass: long-context
+// root with 4 branches at 64 q-heads, chunk 64 (268 MB of fp32 dQ rows per
+// chunk): 108.8 ms head-major vs 115.2 item-major (the full long context:
+// 1,288 vs 1,326 ms at chunk 48); agentic tree, chunk 64 (134 MB): 11.32 vs
+// 11.23 ms; GRPO star, chunk 48 (100 MB): 0.956 vs 0.663 ms.  So head-major
+// above 192 MB of rows per chunk.
+constexpr size_t kHeadMajorRowBytes = 192ull << 20;
 
 void set_cta_order(BwdParams& p, const tree_attn_plan_s* P, const int32_t* chunk_ptr, int hq, int d) {
     p.chunk_ptr = chunk_ptr;

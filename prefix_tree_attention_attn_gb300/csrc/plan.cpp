@@ -222,11 +222,15 @@ int build_plan(const int32_t* parent, const int32_t* seg_len, int32_t n, const t
         // multiples of S, so that the items of every kv-tile that feed the same
         // q-tiles share one chunk index; items run chunk by chunk (then longest
         // first), which keeps the dQ rows they accumulate into resident in L2.
-        // Auto size: 24 q-tiles, doubled while the split kv-tiles would need more
-        // than max(2048, 8 T) partial dK/dV slots.  Short chunks keep the dQ rows
-        // that concurrently running items add into resident in L2 (a sweep on the
-        // long shared-context tree: 2.07 s of backward at 1,775 q-tiles per chunk,
-        // 1.34 s at 32-64); the slot cap bounds the partials' memory.
+        // Auto size: 24 q-tiles below 64 q-tiles, 48 below 256, 64 above, doubled
+        // while the split kv-tiles would need more than max(2048, 8 T) partial
+        // dK/dV slots.  Longer chunks mean fewer partial slots to write and sum
+        // but fewer, longer items to spread over the SMs; measured backward main
+        // pass + partial sum (ms) at 24 / 48 / 64: segment tree (T = 54) 0.396 /
+        // 0.593 / 0.648, GRPO star (T = 88) 0.743 / 0.727 / 0.790, agentic tree
+        // (T = 463) 11.93 / 11.75 / 11.58.  On the long shared-context tree the old
+        // rule (ceil(tile blocks / 600) = 1,775 q-tiles) gave a 2.07 s backward,
+        // 32-96 give 1.28-1.34 s; the slot cap bounds the partials' memory.
         auto slots_for = [&](int64_t S) {
             int64_t n = 0;
             for (int32_t c = 0; c < T; ++c) {
@@ -237,7 +241,7 @@ int build_plan(const int32_t* parent, const int32_t* seg_len, int32_t n, const t
         };
         int64_t S64 = chunk_opt;
         if (S64 <= 0) {
-            S64 = 24;
+            S64 = T < 64 ? 24 : (T < 256 ? 48 : 64);
             while (S64 < T && slots_for(S64) > std::max<int64_t>(2048, 8 * (int64_t)T)) S64 *= 2;
         }
         const int32_t S = (int32_t)std::min<int64_t>(S64, INT32_MAX);

@@ -8,10 +8,12 @@ Element-wise, every row and key:
   turns' keys included;
 * a reduced long shared context: the same 32,768-token root with the first 4
   branches of the long-context recipe (seed 5), one q-head and one kv-head, so
-  that the backward runs as on the full tree (q-range chunks doubled to 48
-  q-tiles, more than 2,048 partial dK/dV slots summed in a fixed order) and
-  every token's O, LSE, dQ, dK and dV -- the root's 32,768 keys included, each
-  summed over hundreds of descendant q-tiles -- is compared with the oracle.
+  that the backward runs as on the full tree (q-range chunks of 64 q-tiles,
+  every root kv-tile split over several items and its partial dK/dV slots
+  summed in a fixed order), and again with chunks of 32 q-tiles (more than
+  3,000 partial slots); every token's O, LSE, dQ, dK and dV -- the root's
+  32,768 keys included, each summed over hundreds of descendant q-tiles -- is
+  compared with the oracle.
 
 For the full trees, beyond those:
 
@@ -186,24 +188,35 @@ def test_agentic_tree_kv_group0_every_token():
 
 def test_long_context_reduced_every_token():
     """32,768-token root + the first 4 branches of the long-context recipe, one
-    head: the backward's doubled chunk rule and > 2,048 partial slots in force,
-    every token compared with the oracle."""
+    head: the backward as the full tree runs it (the automatic chunk of 64
+    q-tiles, every root kv-tile split) and with 32-q-tile chunks (> 3,000
+    partial slots), every token compared with one oracle run."""
     t = WT.long_context_tree(seed=WX.SEEDS["long_context"], branches=4)
-    plan = TreePlan(t.parent, t.seg_len)
-    assert plan.info["bwd_chunk_qtiles"] > 24, plan.info
-    assert plan.info["n_partial_slots"] > 2048, plan.info
-    assert plan.info["n_split_kv_tiles"] >= 256          # every root kv-tile is split
     rec = WX.VALUE_RECIPES["long_context"]
     x = WX.draw_inputs(t.n_tokens, WX.HeadConfig(1, 1, 128), rec, 1000 + WX.SEEDS["long_context"])
     xd = {kk: vv.cuda() for kk, vv in x.items()}
-    o, lse, dq, dk, dv = run(plan, xd["q"], xd["k"], xd["v"], xd["do"], rec.scale)
-    got = {"o": o.float().cpu().numpy(), "lse": lse.cpu().numpy(), "dq": dq.float().cpu().numpy(),
-           "dk": dk.float().cpu().numpy(), "dv": dv.float().cpu().numpy()}
+    full = WT.load_tree("long_context")
+    auto_chunk = TreePlan(full.parent, full.seg_len).info["bwd_chunk_qtiles"]
+    runs = []
+    for chunk in (0, 32):
+        plan = TreePlan(t.parent, t.seg_len, bwd_chunk_qtiles=chunk)
+        if chunk == 0:
+            assert plan.info["bwd_chunk_qtiles"] == auto_chunk > 24, plan.info   # the full tree's chunk
+        else:
+            assert plan.info["n_partial_slots"] > 3000, plan.info
+        assert plan.info["n_split_kv_tiles"] >= 256          # every root kv-tile is split
+        o, lse, dq, dk, dv = run(plan, xd["q"], xd["k"], xd["v"], xd["do"], rec.scale)
+        runs.append((plan.info["bwd_chunk_qtiles"], plan.info["n_partial_slots"],
+                     {"o": o.float().cpu().numpy(), "lse": lse.cpu().numpy(), "dq": dq.float().cpu().numpy(),
+                      "dk": dk.float().cpu().numpy(), "dv": dv.float().cpu().numpy()}))
+        del o, lse, dq, dk, dv
     ref = oracle_all(t, x["q"], x["k"], x["v"], x["do"], rec.scale)
-    compare_all(f"long context, root + 4 branches ({t.n_tokens} tokens), every token", got, ref)
-    # the root prefix's keys on their own: the ones summed over the most q-tiles
     root = slice(0, t.seg_len[0])
-    for name in ("dk", "dv"):
-        e = rel_fro(got[name][root], ref[name][root])
-        print(f"  root-prefix {name}: rel Frobenius {e:.3e}")
-        assert e <= BWD_REL, (name, e)
+    for chunk, slots, got in runs:
+        compare_all(f"long context, root + 4 branches ({t.n_tokens} tokens), chunk {chunk}, {slots} partial "
+                    f"slots, every token", got, ref)
+        # the root prefix's keys on their own: the ones summed over the most q-tiles
+        for name in ("dk", "dv"):
+            e = rel_fro(got[name][root], ref[name][root])
+            print(f"  root-prefix {name}: rel Frobenius {e:.3e}")
+            assert e <= BWD_REL, (name, e)

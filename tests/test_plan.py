@@ -154,3 +154,31 @@ def test_chain_merge_gives_identical_token_plan():
     b = TreePlan([-1], [357]).export()
     for f in ("subend", "qi_ptr", "qi_lo", "qi_hi", "qt_ptr", "qt_kv", "qt_cls", "kv_qlo", "kv_qhi"):
         np.testing.assert_array_equal(a[f], b[f])
+
+
+def expected_chunk(e, T):
+    """The automatic backward chunk as include/tree_attn.h states it: 24 q-tiles
+    below 64 q-tiles, 48 below 256, else 64, doubled while the kv-tiles whose
+    q-range spans several chunks would need more than max(2048, 8 T) slots."""
+    lo, hi = e["kv_qlo"].astype(np.int64), e["kv_qhi"].astype(np.int64)
+
+    def slots(S):
+        n = (hi - 1) // S - lo // S + 1
+        return int(n[n > 1].sum())
+
+    S = 24 if T < 64 else (48 if T < 256 else 64)
+    while S < T and slots(S) > max(2048, 8 * T):
+        S *= 2
+    return S
+
+
+@pytest.mark.parametrize("name", ["tiny_binary", "segment_tree", "grpo_star", "agentic_tree", "long_context",
+                                  "chain"])
+def test_automatic_chunk_rule(lib, name):
+    t = WT.chain_tree([2048 * 128]) if name == "chain" else WT.load_tree(name)
+    p = TreePlan(t.parent, t.seg_len)
+    e = p.export(("kv_qlo", "kv_qhi"))
+    T = p.info["n_qtiles"]
+    assert p.info["bwd_chunk_qtiles"] == expected_chunk(e, T)
+    if name == "chain":        # 2,048 q-tiles of one chain: the slot cap doubles the chunk
+        assert p.info["bwd_chunk_qtiles"] > 64

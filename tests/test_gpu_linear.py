@@ -128,3 +128,25 @@ def test_bwd_timing_segment_tree():
     ms = a.elapsed_time(b) / 10
     print(f"\nlinear bwd segment tree: {ms:.3f} ms, {t.n_tokens / ms / 1e3:.1f} M tokens/s")
     assert all(torch.isfinite(o.float()).all() for o in out)
+
+
+@pytest.mark.parametrize("bad", [0.0, -0.5, 1.5, float("nan")])
+def test_decay_outside_unit_interval_is_reported(bad):
+    """A decay outside (0, 1] lives on the device, so the host cannot refuse it:
+    the forward and the backward record TREE_ATTN_ERR_INVALID_DECAY (-12) in the
+    device status word instead of returning silent NaNs; the next call with a
+    valid decay runs clean."""
+    t = WT.Tree("decay", [-1, 0], [150, 60])
+    x = WX.draw_inputs(t.n_tokens, WX.HeadConfig(2, 2, 128), WX.ValueRecipe(1, 1, 1, 1, 1), 5)
+    plan = TreePlan(t.parent, t.seg_len)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    scale = 1 / np.sqrt(128)
+    dec = torch.tensor([0.9, bad], dtype=torch.float32, device="cuda")
+    tree_linear_fwd(plan, q, k, v, dec, scale)
+    assert device_status() == -12
+    tree_linear_bwd(plan, q, k, v, do, dec, scale)
+    assert device_status() == -12
+    good = torch.tensor([0.9, 1.0], dtype=torch.float32, device="cuda")
+    o = tree_linear_fwd(plan, q, k, v, good, scale)
+    assert device_status() == 0
+    assert torch.isfinite(o.float()).all()

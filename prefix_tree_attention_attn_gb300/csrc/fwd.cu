@@ -264,16 +264,11 @@ __global__ void __launch_bounds__(FwdCfg<D, NS, PER_SM>::NWARPS * 32, PER_SM)
             // thread of the group meets the same named barriers in the same order.
             if (ok) ok = mbar_wait(b_sfull(s), j & 1, p.status, 8);
             ok = __all_sync(0xffffffffu, ok);
-            // When every row of the q-tile lies below every key's subtree end
-            // (q0 + 127 < min subend: a tile on the diagonal of one node, or keys
-            // of an ancestor that all rows descend from), only the causal part of
-            // the mask can remove a key, and the subtree ends are not staged.
-            const bool causal_only = partial && q0 + 127 < kv_min;
             // One barrier publishes the staged subtree ends and makes `ok` uniform.
             // Overwriting the staging row is safe without a barrier before it: S of
             // this tile exists only after every thread of the group has arrived on
             // the previous tile's P barrier, i.e. finished reading the old values.
-            if (partial && !causal_only) {
+            if (partial) {
                 if (ok) sub_sm[r] = my_sub;
                 ok = named_bar_and(1 + s, 128, ok);
             }
@@ -282,19 +277,11 @@ __global__ void __launch_bounds__(FwdCfg<D, NS, PER_SM>::NWARPS * 32, PER_SM)
             // pass 1: row maximum of the raw logits over the 128 key columns.  A warp
             // whose rows all see every key of the tile (j_max <= i < min subend) skips
             // the mask; otherwise masked logits are set to -inf and written back to
-            // TMEM, so pass 2 never masks.  A warp whose rows all come after every
-            // key of the tile (j_max <= i) needs only the subtree-end test.
+            // TMEM, so pass 2 never masks.
             const int kbase = c * 128;
             const bool need_mask =
                 partial && !__all_sync(0xffffffffu, kbase + 127 <= i && i < kv_min);
-            const bool sub_only = !causal_only && __all_sync(0xffffffffu, kbase + 127 <= i);
             auto mask = [&](float (&v)[32], int cc) {
-                if (causal_only) {
-                    const int lim = i - kbase - cc * 32;   // columns u <= lim are kept
-#pragma unroll
-                    for (int u = 0; u < 32; ++u) v[u] = u <= lim ? v[u] : -INFINITY;
-                    return;
-                }
 #pragma unroll
                 for (int u4 = 0; u4 < 8; ++u4) {
                     const int4 sv = reinterpret_cast<const int4*>(sub_sm)[cc * 8 + u4];
@@ -302,7 +289,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NS, PER_SM>::NWARPS * 32, PER_SM)
 #pragma unroll
                     for (int w = 0; w < 4; ++w) {
                         const int u = u4 * 4 + w;
-                        const bool keep = sub_only ? (i < sa[w]) : ((kbase + cc * 32 + u <= i) && (i < sa[w]));
+                        const bool keep = (kbase + cc * 32 + u <= i) && (i < sa[w]);
                         v[u] = keep ? v[u] : -INFINITY;
                     }
                 }

@@ -605,10 +605,16 @@ def run_ours(args):
         e2e_warm = 2 if long_step else max(3, args.warmup)
         side = torch.cuda.Stream(device=dev)        # the dO upload overlaps the forward
 
+        copy_ev = []    # per step: events around the q/k/v upload and the output download
+
         def e2e_step():
             main = torch.cuda.current_stream(dev)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            copy_ev.append(ev)
             # inputs the forward needs first; the plan is built on the host meanwhile
+            ev[0].record(main)
             qd, kd, vd = (pin[n].to(dev, non_blocking=True) for n in ("q", "k", "v"))
+            ev[1].record(main)
             side.wait_stream(main)
             with torch.cuda.stream(side):
                 dod = pin["do"].to(dev, non_blocking=True)   # arrives during the forward
@@ -620,8 +626,10 @@ def run_ours(args):
             # context: 1.90-1.96 s per step this way; 1.93-1.98 s with O and LSE
             # leaving during the backward (the copy slows it); 2.09-2.17 s with
             # device buffers made once and reused.
+            ev[2].record(main)
             for nm, src in (("o", oo), ("lse", ll), ("dq", a), ("dk", b), ("dv", c)):
                 outs[nm].copy_(src, non_blocking=True)
+            ev[3].record(main)
             torch.cuda.synchronize(dev)      # the step's results are on the host
             p2.close()
 
@@ -635,9 +643,15 @@ def run_ours(args):
             e2e_step()
             e2e_each.append(time.perf_counter() - t1)
         e2e_s = (time.perf_counter() - t0) / e2e_steps
+        timed_ev = copy_ev[-e2e_steps:]
+        qkv_bytes = sum(pin[n].numel() * pin[n].element_size() for n in ("q", "k", "v"))
+        h2d_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in timed_ev)
+        d2h_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in timed_ev)
         e2e = {"value": flops_step * world / e2e_s / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3, "steps": e2e_steps,
                "ms_each": [round(t_ * 1e3, 2) for t_ in e2e_each],
+               "qkv_upload_ms": h2d_ms, "qkv_upload_gbs": qkv_bytes / h2d_ms / 1e6,
+               "download_ms": d2h_ms, "download_gbs": d2h / d2h_ms / 1e6,
                "includes": "host plan build + device upload, H2D of q/k/v/dO from pinned memory, fwd+bwd, "
                            "D2H of o/lse/dq/dk/dv after the backward; dO arrives during the forward (side "
                            "stream)"}

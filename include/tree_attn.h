@@ -95,6 +95,13 @@ typedef struct {
                                  than 256, else 64; doubled while the kv-tiles
                                  split over several items would need more than
                                  max(2048, 8 * n_qtiles) partial slots        */
+    int32_t bwd_cta_order;    /* order of the backward's CTAs inside a chunk:
+                                 0 = auto (head-major when a chunk's fp32 dQ
+                                 rows, chunk * 128 * hq * d * 4 bytes, exceed
+                                 192 MB), 1 = item-major (the kv-heads of an
+                                 item side by side), 2 = head-major (every item
+                                 of kv-head 0, then of kv-head 1, ...).  The
+                                 order changes no result bit of dK and dV.    */
 } tree_attn_plan_opts_t;
 
 typedef struct {

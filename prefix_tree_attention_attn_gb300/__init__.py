@@ -40,13 +40,13 @@ class TreePlan:
     """A plan for one rollout tree or forest (``tree_attn_plan``)."""
 
     def __init__(self, parent: Sequence[int], seg_len: Sequence[int], block: int = 0,
-                 bwd_chunk_qtiles: int = 0):
+                 bwd_chunk_qtiles: int = 0, bwd_cta_order: int = 0):
         self._lib = B.load()
         self._h = None
         par, sl = _i32(parent), _i32(seg_len)
         if par.ndim != 1 or sl.shape != par.shape:
             raise ValueError("parent and seg_len must be 1-D arrays of equal length")
-        opts = B.PlanOpts(block, bwd_chunk_qtiles)
+        opts = B.PlanOpts(block, bwd_chunk_qtiles, bwd_cta_order)
         h = C.c_void_p()
         B.check(self._lib.tree_attn_plan(_ptr_i32(par), _ptr_i32(sl), len(par), C.byref(opts), C.byref(h)),
                 "tree_attn_plan")

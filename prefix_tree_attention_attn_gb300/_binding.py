@@ -13,7 +13,7 @@ c_int64_p = C.POINTER(C.c_int64)
 
 
 class PlanOpts(C.Structure):
-    _fields_ = [("block", C.c_int32), ("bwd_chunk_qtiles", C.c_int32)]
+    _fields_ = [("block", C.c_int32), ("bwd_chunk_qtiles", C.c_int32), ("bwd_cta_order", C.c_int32)]
 
 
 class PlanInfo(C.Structure):

@@ -207,7 +207,8 @@ void set_cta_order(BwdParams& p, const tree_attn_plan_s* P, const int32_t* chunk
     p.chunk_ptr = chunk_ptr;
     p.n_chunks = (int32_t)P->chunk_ptr.size() - 1;
     const size_t rows = (size_t)P->chunk * kBlock * hq * d * 4;
-    p.head_major = (rows > kHeadMajorRowBytes && p.n_chunks > 0) ? 1 : 0;
+    const bool head_major = P->cta_order == 0 ? rows > kHeadMajorRowBytes : P->cta_order == 2;
+    p.head_major = (head_major && p.n_chunks > 0) ? 1 : 0;
 }
 
 }  // namespace

@@ -43,12 +43,13 @@ int build_plan(const int32_t* parent, const int32_t* seg_len, int32_t n, const t
     if (!parent || !seg_len || !out || n <= 0) return TREE_ATTN_ERR_INVALID_ARG;
     *out = nullptr;
     int32_t B = 128;
-    int32_t chunk_opt = 0;
+    int32_t chunk_opt = 0, order_opt = 0;
     if (opts) {
         if (opts->block != 0) B = opts->block;
         chunk_opt = opts->bwd_chunk_qtiles;
+        order_opt = opts->bwd_cta_order;
     }
-    if (B < 1 || B > 1024 || chunk_opt < 0) return TREE_ATTN_ERR_INVALID_ARG;
+    if (B < 1 || B > 1024 || chunk_opt < 0 || order_opt < 0 || order_opt > 2) return TREE_ATTN_ERR_INVALID_ARG;
 
     // ---- validate -----------------------------------------------------------
     int64_t N = 0;
@@ -63,6 +64,7 @@ int build_plan(const int32_t* parent, const int32_t* seg_len, int32_t n, const t
     if (!P) return TREE_ATTN_ERR_OUT_OF_MEMORY;
     try {
         P->n_nodes = n;
+        P->cta_order = order_opt;
         P->parent.assign(parent, parent + n);
         P->seg_len.assign(seg_len, seg_len + n);
         P->block = B;

@@ -69,6 +69,7 @@ struct Plan {
     int64_t pairs = 0;
     int64_t n_full = 0;
     int32_t chunk = 0;
+    int32_t cta_order = 0;   // backward CTA order: 0 auto, 1 item-major, 2 head-major
     std::vector<int32_t> node_order, node_off, subend;
     std::vector<int32_t> qi_ptr, qi_lo, qi_hi;
     std::vector<int32_t> qt_ptr, qt_kv;

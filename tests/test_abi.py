@@ -42,7 +42,7 @@ def plan_status(lib, parent, seg_len, block=0, chunk=0):
     par = np.asarray(parent, dtype=np.int32)
     sl = np.asarray(seg_len, dtype=np.int32)
     h = C.c_void_p()
-    opts = B.PlanOpts(block, chunk)
+    opts = B.PlanOpts(block, chunk, 0)
     st = lib.tree_attn_plan(par.ctypes.data_as(B.c_int32_p), sl.ctypes.data_as(B.c_int32_p), len(par),
                             C.byref(opts), C.byref(h))
     if st == 0:
@@ -68,6 +68,10 @@ def test_invalid_options_and_sizes(lib):
     assert plan_status(lib, [-1], [4], block=-3) == -1
     assert plan_status(lib, [-1], [4], block=2048) == -1
     assert plan_status(lib, [-1], [4], chunk=-1) == -1
+    for bad in (-1, 3):
+        par, sl, h = np.asarray([-1], dtype=np.int32), np.asarray([4], dtype=np.int32), C.c_void_p()
+        assert lib.tree_attn_plan(par.ctypes.data_as(B.c_int32_p), sl.ctypes.data_as(B.c_int32_p), 1,
+                                  C.byref(B.PlanOpts(0, 0, bad)), C.byref(h)) == -1
     assert plan_status(lib, [-1, 0], [2**30, 2**30]) == -3      # token count overflows int32
     h = C.c_void_p()
     assert lib.tree_attn_plan(None, None, 1, None, C.byref(h)) == -1

@@ -59,7 +59,7 @@ def test_random_trees(seed):
     full_parity(t, q, k, v, do, 1 / np.sqrt(d), tag=f"seed{seed}")
 
 
-@pytest.mark.parametrize("heads", [(4, 2, 128), (3, 1, 128)])
+@pytest.mark.parametrize("heads", [(4, 2, 128), (3, 1, 128), (4, 2, 64), (3, 1, 64), (16, 2, 128)])
 def test_long_kv_lists(heads):
     """A tree whose q-tiles see more than 24 kv-tiles on average: the forward
     then runs its long-list shapes (two q-heads per CTA for an even group size,
@@ -113,3 +113,24 @@ def test_backward_dk_dv_bitwise_reproducible():
     _, dk2, dv2 = tree_attn_bwd(plan, q, k, v, o, lse, do, rec.scale)
     torch.cuda.synchronize()
     assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
+
+
+@pytest.mark.parametrize("order", [1, 2])
+def test_backward_cta_orders(order):
+    """Both backward CTA orders against the oracle (the automatic rule picks
+    head-major only for chunks with over 192 MB of dQ rows, i.e. the long
+    context), on trees whose kv-tiles split over several chunks and several
+    kv-heads; dK and dV are the same bits in either order."""
+    t = WT.Tree("orders", [-1, 0, 0, 1, 2], [900, 300, 500, 129, 200])
+    hq, hkv, d = 8, 2, 128
+    q, k, v, do = draw(t.n_tokens, hq, hkv, d, seed=41)
+    scale = 1 / np.sqrt(d)
+    plan = TreePlan(t.parent, t.seg_len, bwd_chunk_qtiles=4, bwd_cta_order=order)
+    assert plan.info["n_split_kv_tiles"] > 0
+    _, g = run_gpu(t, q, k, v, do, scale, plan=plan)
+    from oracle import attention as OA
+    rg = OA.backward(t.parent, t.seg_len, q, k, v, do, scale)
+    assert_bwd((g["dq"], g["dk"], g["dv"]), rg, f"order {order}")
+    other = TreePlan(t.parent, t.seg_len, bwd_chunk_qtiles=4, bwd_cta_order=3 - order)
+    _, g2 = run_gpu(t, q, k, v, do, scale, plan=other)
+    assert np.array_equal(g["dk"], g2["dk"]) and np.array_equal(g["dv"], g2["dv"])

@@ -134,3 +134,19 @@ def test_backward_cta_orders(order):
     other = TreePlan(t.parent, t.seg_len, bwd_chunk_qtiles=4, bwd_cta_order=3 - order)
     _, g2 = run_gpu(t, q, k, v, do, scale, plan=other)
     assert np.array_equal(g["dk"], g2["dk"]) and np.array_equal(g["dv"], g2["dv"])
+
+
+def test_d64_backward_with_split_items():
+    """head_dim 64 with short chunks, so kv-tiles split over several items and
+    the fixed-order partial sum runs at d = 64 too."""
+    t = WT.Tree("d64split", [-1, 0, 0, 2], [700, 260, 400, 300])
+    hq, hkv, d = 4, 2, 64
+    q, k, v, do = draw(t.n_tokens, hq, hkv, d, seed=43)
+    scale = 1 / np.sqrt(d)
+    plan = TreePlan(t.parent, t.seg_len, bwd_chunk_qtiles=2)
+    assert plan.info["n_split_kv_tiles"] > 0 and plan.info["n_partial_slots"] > 0
+    _, g = run_gpu(t, q, k, v, do, scale, plan=plan)
+    from oracle import attention as OA
+    ro, rl = OA.forward(t.parent, t.seg_len, q, k, v, scale)
+    assert_fwd(g["o"], g["lse"], ro, rl, "d64 split")
+    assert_bwd((g["dq"], g["dk"], g["dv"]), OA.backward(t.parent, t.seg_len, q, k, v, do, scale), "d64 split")

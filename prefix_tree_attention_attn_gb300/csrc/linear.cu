@@ -36,10 +36,74 @@ constexpr int kChunk = 128;
 constexpr int kD = 128;
 constexpr int kTile = kChunk * kD * 2;   // 32 KB bf16 tile
 
+__device__ __forceinline__ void st_shared_v2_b32(uint32_t addr, uint32_t a, uint32_t b) {
+    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+
+__device__ __forceinline__ void bulk_store_s2g(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
+}
+
+// A 128 x 128 fp32 TMEM accumulator (TMEM lane = row) -> 128 contiguous fp32
+// rows of 512 bytes at `dst`, by warps 0-3 (32 rows each).  Each thread stages
+// its row in shared memory at a 528-byte row stride (16 bytes more than a row,
+// so the 32 rows of a warp fall on different bank groups); lane 0 of each warp
+// then copies the warp's rows out with one bulk copy per row, so rows leave as
+// whole lines rather than as one 16-byte piece of 32 rows per store.
+constexpr uint32_t kRowStage = 528;
+constexpr int kRowStageBytes = 128 * kRowStage;
+
+__device__ __forceinline__ void store_rows_f32(uint32_t tmem_rows, uint32_t stage, float* __restrict__ dst, int warp,
+                                               int lane) {
+    const uint32_t my = stage + (uint32_t)(warp * 32 + lane) * kRowStage;
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+        float v[32];
+        tmem_ld32(tmem_rows + cc * 32, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            st_shared_v4(my + cc * 128 + q * 16, __float_as_uint(v[4 * q]), __float_as_uint(v[4 * q + 1]),
+                         __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3]));
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        for (int rr = 0; rr < 32; ++rr) {
+            const int row = warp * 32 + rr;
+            bulk_store_s2g(dst + (size_t)row * 128, stage + (uint32_t)row * kRowStage, 512);
+        }
+        bulk_commit();
+        bulk_wait_all();
+    }
+    __syncwarp();
+}
+
+// An fp32 d x d state (row = key feature, fp32 [key feature][value feature])
+// -> a bf16 tile at `dst` laid out like a value tile (two 64-column
+// 128B-swizzled blocks).  Warps 0 .. kRows/128-1 take kRows rows each and read
+// one row per instruction (512 contiguous bytes, lane l holding features
+// 4l .. 4l+3), so every global load is fully used; lane l then writes its 8
+// bytes into the 16-byte piece ((l & 15) >> 1) of block (l >> 4), two
+// wavefronts per row.
+template <int kRows>
+__device__ __forceinline__ void stage_state_bf16(const float* __restrict__ state, uint32_t dst, int warp, int lane) {
+    const float4* src = reinterpret_cast<const float4*>(state);
+    const uint32_t blk = lane >> 4, cj = (lane & 15) >> 1, half = lane & 1;
+#pragma unroll 16
+    for (int rr = 0; rr < kRows; ++rr) {   // 16 rows' loads in flight
+        const int row = warp * kRows + rr;
+        const float4 a4 = src[row * 32 + lane];
+        st_shared_v2_b32(dst + blk * 16384 + sw128_offset(row, cj) + half * 8, pack_bf16x2(a4.x, a4.y),
+                         pack_bf16x2(a4.z, a4.w));
+    }
+}
+
 // ---- dS per (chunk, kv-head) -------------------------------------------------
 // warps 0-3: lane r = token row r (scaling V) and key feature r (read-out);
 // warp 4: TMEM owner, lane 0 issues the loads and the MMA.
-constexpr int kDeltaSmem = 1024 + 2 * kTile;
+constexpr int kDeltaSmem = 1024 + kRowStageBytes;   // K, V; then the fp32 staging rows over them
 
 __global__ void __launch_bounds__(160, 1)
     lin_delta_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -90,12 +154,15 @@ __global__ void __launch_bounds__(160, 1)
             uint4* row = reinterpret_cast<uint4*>(smem + 1024 + kTile + blk * 16384 + r * 128);
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                uint4 x = row[c];
+                // the row's 16-byte pieces in an order rotated by the row, so that the
+                // 32 rows of a warp spread over every bank group instead of one
+                const int cr = (c + r) & 7;
+                uint4 x = row[cr];
                 uint32_t* u = reinterpret_cast<uint32_t*>(&x);
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     u[e] = pack_bf16x2(__uint_as_float(u[e] << 16) * w, __uint_as_float(u[e] & 0xffff0000u) * w);
-                row[c] = x;
+                row[cr] = x;
             }
         }
         fence_proxy_async_smem();
@@ -115,18 +182,10 @@ __global__ void __launch_bounds__(160, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (ok) {
             tc_fence_after();
-            const int r = threadIdx.x;   // key feature
-            const uint32_t lane_base = tmem + ((uint32_t)(warp << 5) << 16);
-            float4* dst = reinterpret_cast<float4*>(ds + (((size_t)chunk * hkv + g) * kD + r) * kD);
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                float v[32];
-                tmem_ld32(lane_base + cc * 32, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    dst[cc * 8 + u] = make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
-            }
+            // row = key feature; K and V have been read by the product, so their
+            // tiles hold the staging rows
+            store_rows_f32(tmem + ((uint32_t)(warp << 5) << 16), sb + 1024, ds + ((size_t)chunk * hkv + g) * kD * kD,
+                           warp, threadIdx.x & 31);
         }
     }
     tc_fence_before();
@@ -137,26 +196,59 @@ __global__ void __launch_bounds__(160, 1)
     }
 }
 
-// ---- entering states, node by node in packed order ----------------------------
-__global__ void __launch_bounds__(256) lin_scan_kernel(const int32_t* __restrict__ lnodes, int n_nodes,
+// ---- entering states, chunk by chunk in packed order -------------------------
+// One thread per (state entry, kv-head) walks every chunk of the tree in packed
+// order; a node's chunks are consecutive, and a node's first chunk starts from
+// its parent's exit state (0 at a root), which is final by then because the
+// parent precedes the node.  With one thread per entry there are few threads
+// per SM, so each keeps kScanBatch increments in flight (loaded before the
+// recurrence uses the first of them); chunk lengths and node ids, the same for
+// every thread, are staged in shared memory a window at a time.
+constexpr int kScanBatch = 16;
+constexpr int kScanWin = 1024;
+
+__global__ void __launch_bounds__(256) lin_scan_kernel(const int32_t* __restrict__ lnodes, int n_chunks,
                                                      const int32_t* __restrict__ chunks,
                                                      const float* __restrict__ decay, int hkv,
                                                      const float* __restrict__ ds, float* __restrict__ s_in,
                                                      float* __restrict__ s_out) {
+    __shared__ int w_len[kScanWin], w_node[kScanWin];
     const int e = blockIdx.x * blockDim.x + threadIdx.x;   // state entry (row * d + col)
     const int g = blockIdx.y;
     const size_t dd = (size_t)kD * kD;
     const float lg = log2f(decay[g]);
-    for (int k = 0; k < n_nodes; ++k) {
-        const int par = lnodes[4 * k], c0 = lnodes[4 * k + 1], nc = lnodes[4 * k + 2];
-        float S = par < 0 ? 0.f : s_out[((size_t)par * hkv + g) * dd + e];
-        for (int c = c0; c < c0 + nc; ++c) {
-            const size_t at = ((size_t)c * hkv + g) * dd + e;
-            s_in[at] = S;
-            S = exp2f((float)chunks[4 * c + 1] * lg) * S + ds[at];
+    float S = 0.f;
+    int cur = -1;   // the node whose chunks are being walked
+    for (int w0 = 0; w0 < n_chunks; w0 += kScanWin) {
+        const int nw = min(kScanWin, n_chunks - w0);
+        __syncthreads();   // the previous window has been read
+        for (int t = threadIdx.x; t < nw; t += blockDim.x) {
+            w_len[t] = chunks[4 * (w0 + t) + 1];
+            w_node[t] = chunks[4 * (w0 + t) + 2];
         }
-        s_out[((size_t)k * hkv + g) * dd + e] = S;
+        __syncthreads();
+        for (int c = 0; c < nw; c += kScanBatch) {
+            float dsv[kScanBatch];
+#pragma unroll
+            for (int u = 0; u < kScanBatch; ++u)
+                if (c + u < nw) dsv[u] = ds[((size_t)(w0 + c + u) * hkv + g) * dd + e];
+#pragma unroll
+            for (int u = 0; u < kScanBatch; ++u)
+                if (c + u < nw) {
+                    const int node = w_node[c + u];
+                    if (node != cur) {   // first chunk of a node
+                        const int par = lnodes[4 * node];
+                        if (cur >= 0) s_out[((size_t)cur * hkv + g) * dd + e] = S;
+                        // the node right after its parent continues from S itself
+                        if (par != cur) S = par < 0 ? 0.f : s_out[((size_t)par * hkv + g) * dd + e];
+                        cur = node;
+                    }
+                    s_in[((size_t)(w0 + c + u) * hkv + g) * dd + e] = S;
+                    S = exp2f((float)w_len[c + u] * lg) * S + dsv[u];
+                }
+        }
     }
+    if (cur >= 0) s_out[((size_t)cur * hkv + g) * dd + e] = S;
 }
 
 // ---- outputs per (chunk, kv-head): the group's q-heads one after another ------
@@ -164,11 +256,18 @@ __global__ void __launch_bounds__(256) lin_scan_kernel(const int32_t* __restrict
 // group; Q comes through two slots and TMEM holds two heads (S / P at
 // [256b, 256b + 128), O at [256b + 128, 256b + 256) for buffer b = head & 1), so
 // one head's P and output overlap the next head's S and Q S_in products.
-// warps 0-3: lane m = query row m (and key feature m when staging S_in);
-// warp 4: loads; warp 5: TMEM owner, lane 0 issues the MMAs.
-constexpr int kOutSmem = 1024 + 5 * kTile;   // K, V, S_in (bf16), Q x 2
+// warps 0-7: query row m = 32 (w % 4) + lane (the TMEM lanes warp w may
+// access), columns [64 (w / 4), 64 (w / 4) + 64) of S and of O -- two warps per
+// row, so that each SM sub-partition has two warps of element-wise work; P of
+// columns [64 j, 64 j + 64) is packed at [64 j, 64 j + 32), over columns the
+// same warps have read.  warp 8: loads; warp 9: TMEM owner, lane 0 issues the
+// MMAs.  The decay mask gamma^(m - m') depends on m - m' alone: its 128 values
+// (and zeros for m' > m) are tabulated once per CTA in shared memory.
+constexpr int kOutSmem = 2048 + 5 * kTile;   // barriers, mask table, K, V, S_in (bf16), Q x 2
+constexpr int kLinWarps = 10;                // 8 element-wise warps, loader, MMA issuer
+constexpr int kLinThreads = 32 * kLinWarps;
 
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kLinThreads, 1)
     lin_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const int32_t* __restrict__ chunks,
                    const float* __restrict__ decay, const float* __restrict__ s_in, uint16_t* __restrict__ out,
@@ -194,29 +293,35 @@ __global__ void __launch_bounds__(192, 1)
     auto b_o2 = [&](int b) { return bar(12 + b); };
     auto b_oe = [&](int b) { return bar(14 + b); };
     const uint32_t b_drain = bar(16), holder = bar(17);
-    const uint32_t ka = sb + 1024, va = ka + kTile, sina = va + kTile, qa0 = sina + kTile;
+    const uint32_t ka = sb + 2048, va = ka + kTile, sina = va + kTile, qa0 = sina + kTile;
+    // mtab[128 + t] = gamma^t for t = m - m' in [0, 128), 0 for t < 0
+    float* mtab = reinterpret_cast<float*>(smem + 1024);
+    if (threadIdx.x < 128) {
+        mtab[threadIdx.x] = 0.f;
+        mtab[128 + threadIdx.x] = exp2f((float)threadIdx.x * log2f(decay[g]));
+    }
     if (threadIdx.x == 0) {
         mbar_init(b_kv, 1);
-        mbar_init(b_sin, 128);
+        mbar_init(b_sin, 256);
         for (int b = 0; b < 2; ++b) {
             mbar_init(b_qf(b), 1);
             mbar_init(b_qe(b), 1);
             mbar_init(b_sf(b), 1);
             mbar_init(b_o1(b), 1);
-            mbar_init(b_p(b), 128);
+            mbar_init(b_p(b), 256);
             mbar_init(b_o2(b), 1);
-            mbar_init(b_oe(b), 128);
+            mbar_init(b_oe(b), 256);
         }
         mbar_init(b_drain, 1);
         fence_mbar_init();
     }
-    if (warp == 5) tmem_alloc(holder, 512);
+    if (warp == 9) tmem_alloc(holder, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + 8 * 17);
 
-    if (warp == 4) {
+    if (warp == 8) {
         if (lane == 0) {
             mbar_expect_tx(b_kv, 2 * kTile);
             for (int blk = 0; blk < 2; ++blk) {
@@ -233,7 +338,7 @@ __global__ void __launch_bounds__(192, 1)
                     tma_load_3d(qa0 + b * kTile + blk * 16384, &tm_q, blk * 64, g * G + n, off, b_qf(b));
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         if (lane == 0) {
             constexpr uint32_t ID_S = idesc_bf16(128, 128, false, false);   // Q K^T
             constexpr uint32_t ID_O = idesc_bf16(128, 128, false, true);    // Q S_in, P V
@@ -243,9 +348,9 @@ __global__ void __launch_bounds__(192, 1)
                 const int b = n & 1;
                 tc_fence_after();
 #pragma unroll
-                for (int k = 0; k < kChunk / 16; ++k)
-                    mma_bf16_ts(tmem + 256 * b + 128, tmem + 256 * b + k * 8, sdesc_sw128(va + k * 2048, 16384, 1024),
-                                ID_O, 1u);
+                for (int k = 0; k < kChunk / 16; ++k)   // keys 16k .. 16k + 15 packed at 64 (k / 4) + 8 (k % 4)
+                    mma_bf16_ts(tmem + 256 * b + 128, tmem + 256 * b + (k >> 2) * 64 + (k & 3) * 8,
+                                sdesc_sw128(va + k * 2048, 16384, 1024), ID_O, 1u);
                 mma_commit(b_o2(b));
             };
             for (int n = 0; n < G && ok; ++n) {
@@ -285,23 +390,15 @@ __global__ void __launch_bounds__(192, 1)
         }
         __syncwarp();
     } else {
-        const int m = threadIdx.x;   // query row; key feature when staging the state
-        const uint32_t lane_base = tmem + ((uint32_t)(warp << 5) << 16);
+        const int m = ((warp & 3) << 5) + lane;   // query row; key feature when staging the state
+        const int col0 = (warp >> 2) * 64;         // this warp's 64 columns of S and of O
+        const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) << 5) << 16);
         const float lg = log2f(decay[g]);
         // S_in (fp32, [key feature][value feature]) -> bf16 B operand, laid out
         // like a value tile: row = key feature, two 64-column 128B-swizzled blocks
-        {
-            const float4* src = reinterpret_cast<const float4*>(s_in + (((size_t)chunk * hkv + g) * kD + m) * kD);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {   // 8 features per 16-byte chunk
-                const float4 a4 = src[2 * j], b4 = src[2 * j + 1];
-                const int blk = j >> 3, cj = j & 7;
-                st_shared_v4(sina + blk * 16384 + sw128_offset(m, cj), pack_bf16x2(a4.x, a4.y),
-                             pack_bf16x2(a4.z, a4.w), pack_bf16x2(b4.x, b4.y), pack_bf16x2(b4.z, b4.w));
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(b_sin);
-        }
+        stage_state_bf16<16>(s_in + ((size_t)chunk * hkv + g) * kD * kD, sina, warp, lane);
+        fence_proxy_async_smem();
+        mbar_arrive(b_sin);
         const float fo = scale * exp2f((float)(m + 1) * lg);   // weight of the carried-in part
         bool ok = true;
         for (int n = 0; n < G; ++n) {
@@ -311,22 +408,21 @@ __global__ void __launch_bounds__(192, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (ok) {
                 tc_fence_after();
-                // P[m, m'] = scale * S[m, m'] * gamma^(m - m') for m' <= m and m' < L
+                // P[m, m'] = scale * S[m, m'] * gamma^(m - m') for m' <= m (rows m >= L
+                // are never stored, and for m < L every m' <= m lies in the chunk)
+                const float* wt = mtab + 128 + m;   // wt[-m'] = gamma^(m - m'), 0 past the diagonal
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
+                for (int cc = 0; cc < 2; ++cc) {
                     float v[32];
-                    tmem_ld32(tS + cc * 32, v);
+                    tmem_ld32(tS + col0 + cc * 32, v);
                     tmem_wait_ld();
                     uint32_t pw[16];
 #pragma unroll
                     for (int w = 0; w < 16; ++w) {
-                        const int c0 = cc * 32 + 2 * w, c1 = c0 + 1;
-                        const float p0 = (c0 <= m && c0 < L) ? scale * v[2 * w] * exp2f((float)(m - c0) * lg) : 0.f;
-                        const float p1 =
-                            (c1 <= m && c1 < L) ? scale * v[2 * w + 1] * exp2f((float)(m - c1) * lg) : 0.f;
-                        pw[w] = pack_bf16x2(p0, p1);
+                        const int c0 = col0 + cc * 32 + 2 * w, c1 = c0 + 1;
+                        pw[w] = pack_bf16x2(scale * v[2 * w] * wt[-c0], scale * v[2 * w + 1] * wt[-c1]);
                     }
-                    tmem_st16(tS + cc * 16, pw);
+                    tmem_st16(tS + col0 + cc * 16, pw);
                 }
                 tmem_wait_st();
                 ok = mbar_wait(b_o1(b), u & 1, status, 87);
@@ -335,13 +431,13 @@ __global__ void __launch_bounds__(192, 1)
             if (ok) {
                 tc_fence_after();
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
+                for (int cc = 0; cc < 2; ++cc) {
                     float v[32];
-                    tmem_ld32(tO + cc * 32, v);
+                    tmem_ld32(tO + col0 + cc * 32, v);
                     tmem_wait_ld();
 #pragma unroll
                     for (int w = 0; w < 32; ++w) v[w] *= fo;
-                    tmem_st32(tO + cc * 32, v);
+                    tmem_st32(tO + col0 + cc * 32, v);
                 }
                 tmem_wait_st();
                 tc_fence_before();
@@ -351,11 +447,11 @@ __global__ void __launch_bounds__(192, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (ok) {
                 tc_fence_after();
-                uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)(off + m) * hq + h) * kD);
+                uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)(off + m) * hq + h) * kD + col0);
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
+                for (int cc = 0; cc < 2; ++cc) {
                     float v[32];
-                    tmem_ld32(tO + cc * 32, v);
+                    tmem_ld32(tO + col0 + cc * 32, v);
                     tmem_wait_ld();
                     if (m < L) {
 #pragma unroll
@@ -376,7 +472,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -471,7 +567,7 @@ LinWs lin_layout(const tree_attn_plan_s* P, int32_t hkv) {
 // ---- F per (chunk, kv-head), the group's q-heads accumulated in TMEM ----------
 // warps 0-3: lane r = token row r (scaling dO) and key feature r (read-out);
 // warp 4: TMEM owner, lane 0 loads and issues.
-constexpr int kAdjSmem = 1024 + 2 * kTile;
+constexpr int kAdjSmem = 1024 + kRowStageBytes;   // Q, dO; then the fp32 staging rows over them
 
 __global__ void __launch_bounds__(160, 1)
     lin_bwd_f_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -525,13 +621,14 @@ __global__ void __launch_bounds__(160, 1)
                     uint4* row = reinterpret_cast<uint4*>(smem + 1024 + kTile + blk * 16384 + r * 128);
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
-                        uint4 x = row[c];
+                        const int cr = (c + r) & 7;   // rotated by the row: no bank conflicts
+                        uint4 x = row[cr];
                         uint32_t* u = reinterpret_cast<uint32_t*>(&x);
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
                             u[e] = pack_bf16x2(__uint_as_float(u[e] << 16) * w,
                                                __uint_as_float(u[e] & 0xffff0000u) * w);
-                        row[c] = x;
+                        row[cr] = x;
                     }
                 }
                 fence_proxy_async_smem();
@@ -556,18 +653,10 @@ __global__ void __launch_bounds__(160, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (ok) {
             tc_fence_after();
-            const int r = threadIdx.x;   // key feature
-            const uint32_t lane_base = tmem + ((uint32_t)(warp << 5) << 16);
-            float4* dst = reinterpret_cast<float4*>(f_out + (((size_t)chunk * hkv + g) * kD + r) * kD);
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                float v[32];
-                tmem_ld32(lane_base + cc * 32, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    dst[cc * 8 + u] = make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
-            }
+            // row = key feature; the last head's Q and dO have been read, so their
+            // tiles hold the staging rows
+            store_rows_f32(tmem + ((uint32_t)(warp << 5) << 16), sb + 1024,
+                           f_out + ((size_t)chunk * hkv + g) * kD * kD, warp, threadIdx.x & 31);
         }
     }
     tc_fence_before();
@@ -578,12 +667,16 @@ __global__ void __launch_bounds__(160, 1)
     }
 }
 
-// ---- adjoints, node by node in reverse packed order --------------------------
+// ---- adjoints, chunk by chunk in reverse packed order ------------------------
 // One thread per (state entry, kv-head).  A node's children come after it in
-// packed order, so walking backwards every child's entering adjoint has been
-// added into its parent's slot (csum) before the parent is reached.
+// packed order, so walking the chunks backwards every child's entering adjoint
+// has been added into its parent's slot (csum) before the parent's last chunk
+// is reached.  kBwdScanBatch adjoint increments are loaded at a time, as in the
+// forward scan (a smaller batch here measured faster than the forward's).
+constexpr int kBwdScanBatch = 8;
+
 __global__ void __launch_bounds__(256) lin_bwd_scan_kernel(const int32_t* __restrict__ lnodes, int n_nodes,
-                                                         const int32_t* __restrict__ chunks,
+                                                         int n_chunks, const int32_t* __restrict__ chunks,
                                                          const float* __restrict__ decay, int hkv,
                                                          const float* __restrict__ f_in, float* __restrict__ rsum,
                                                          float* __restrict__ csum) {
@@ -592,26 +685,56 @@ __global__ void __launch_bounds__(256) lin_bwd_scan_kernel(const int32_t* __rest
     const size_t dd = (size_t)kD * kD;
     const float lg = log2f(decay[g]);
     for (int k = 0; k < n_nodes; ++k) csum[((size_t)k * hkv + g) * dd + e] = 0.f;
-    for (int k = n_nodes - 1; k >= 0; --k) {
-        const int par = lnodes[4 * k], c0 = lnodes[4 * k + 1], nc = lnodes[4 * k + 2];
-        float acc = csum[((size_t)k * hkv + g) * dd + e];   // sum over the children's entering adjoints
-        for (int c = c0 + nc - 1; c >= c0; --c) {
-            const size_t at = ((size_t)c * hkv + g) * dd + e;
-            rsum[at] = acc;
-            acc = f_in[at] + exp2f((float)chunks[4 * c + 1] * lg) * acc;
-        }
+    float acc = 0.f;
+    int cur = -1;   // the node whose chunks are being walked
+    for (int c = n_chunks - 1; c >= 0; c -= kBwdScanBatch) {
+        float fv[kBwdScanBatch];
+        int len[kBwdScanBatch], node[kBwdScanBatch];
+#pragma unroll
+        for (int u = 0; u < kBwdScanBatch; ++u)
+            if (c - u >= 0) {
+                fv[u] = f_in[((size_t)(c - u) * hkv + g) * dd + e];
+                len[u] = chunks[4 * (c - u) + 1];
+                node[u] = chunks[4 * (c - u) + 2];
+            }
+#pragma unroll
+        for (int u = 0; u < kBwdScanBatch; ++u)
+            if (c - u >= 0) {
+                if (node[u] != cur) {   // last chunk of a node: start from its children's sum
+                    if (cur >= 0) {
+                        const int par = lnodes[4 * cur];
+                        if (par >= 0) csum[((size_t)par * hkv + g) * dd + e] += acc;
+                    }
+                    cur = node[u];
+                    acc = csum[((size_t)cur * hkv + g) * dd + e];
+                }
+                rsum[((size_t)(c - u) * hkv + g) * dd + e] = acc;
+                acc = fv[u] + exp2f((float)len[u] * lg) * acc;
+            }
+    }
+    if (cur >= 0) {
+        const int par = lnodes[4 * cur];
         if (par >= 0) csum[((size_t)par * hkv + g) * dd + e] += acc;
     }
 }
 
 // ---- dK, dV per (chunk, kv-head) ------------------------------------------------
 // TMEM: dK [0, 128), dV [128, 256), S^T -> P^T [256, 384), A^T -> dA^T [384, 512).
-// warps 0-3: lane m' = key row m' (and key feature when staging Rsum); warp 4:
-// loads; warp 5: TMEM owner, lane 0 issues the MMAs.  The group's q-heads run
-// one after another through one Q / dO slot pair.
-constexpr int kKvSmem = 1024 + 5 * kTile;   // K, V, Rsum (bf16), Q, dO
+// warps 0-7: key row m' = 32 (w % 4) + lane (the TMEM lanes warp w may access);
+// warp w < 4 takes queries [0, 64) of S^T and A^T (packed over their first 32
+// columns) and dK, warp w >= 4 queries [64, 128) (packed at [64, 96)) and dV;
+// warp 8: loads; warp 9: TMEM owner, lane 0 issues the MMAs.  The group's q-heads run
+// one after another through two Q / dO slot pairs, so the next head's tiles
+// arrive while the current head is worked on; its S^T and A^T products are
+// issued right after the current head's dV and dK products, which the tensor
+// core completes first (products issued by one thread run in issue order), so
+// P^T and dA^T are read before they are overwritten.  The two query halves are
+// masked by different warps, and each half's dV and dK products start as soon
+// as that half is done.  The mask weight
+// scale * gamma^(m - m') depends on m - m' alone and is tabulated per CTA.
+constexpr int kKvSmem = 2048 + 7 * kTile;   // barriers, mask table, K, V, Rsum (bf16), (Q, dO) x 2
 
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kLinThreads, 1)
     lin_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                       const int32_t* __restrict__ chunks, const float* __restrict__ decay,
@@ -628,29 +751,42 @@ __global__ void __launch_bounds__(192, 1)
     const int chunk = blockIdx.x / hkv, g = blockIdx.x % hkv;
     const int off = chunks[4 * chunk], L = chunks[4 * chunk + 1];
     auto bar = [&](int i) { return sb + 8u * (uint32_t)i; };
-    const uint32_t b_kv = bar(0), b_r = bar(1), b_inter = bar(2), b_scaled = bar(3), b_qf = bar(4), b_sa = bar(5),
-                   b_pa = bar(6), b_qe = bar(7), b_done = bar(8), b_drain = bar(9), holder = bar(10);
-    const uint32_t ka = sb + 1024, va = ka + kTile, ra = va + kTile, qa = ra + kTile, da = qa + kTile;
+    const uint32_t b_kv = bar(0), b_r = bar(1), b_inter = bar(2), b_scaled = bar(3), b_sa = bar(8), b_done = bar(11),
+                   b_drain = bar(12), holder = bar(13);
+    auto b_qf = [&](int b) { return bar(4 + b); };   // slot b's Q and dO have arrived
+    auto b_qe = [&](int b) { return bar(6 + b); };   // slot b's Q and dO have been read
+    auto b_pa = [&](int h) { return bar(9 + h); };   // query half h masked
+    const uint32_t ka = sb + 2048, va = ka + kTile, ra = va + kTile;
+    auto qa = [&](int b) { return ra + kTile + 2u * kTile * (uint32_t)b; };
+    auto da = [&](int b) { return qa(b) + kTile; };
+    // wtab[128 + t] = scale * gamma^t for t = m - m' in [0, 128), 0 for t < 0
+    float* wtab = reinterpret_cast<float*>(smem + 1024);
+    if (threadIdx.x < 128) {
+        wtab[threadIdx.x] = 0.f;
+        wtab[128 + threadIdx.x] = scale * exp2f((float)threadIdx.x * log2f(decay[g]));
+    }
     if (threadIdx.x == 0) {
         mbar_init(b_kv, 1);
-        mbar_init(b_r, 128);
+        mbar_init(b_r, 256);
         mbar_init(b_inter, 1);
-        mbar_init(b_scaled, 128);
-        mbar_init(b_qf, 1);
+        mbar_init(b_scaled, 256);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(b_qf(b), 1);
+            mbar_init(b_qe(b), 1);
+            mbar_init(b_pa(b), 128);
+        }
         mbar_init(b_sa, 1);
-        mbar_init(b_pa, 128);
-        mbar_init(b_qe, 1);
         mbar_init(b_done, 1);
         mbar_init(b_drain, 1);
         fence_mbar_init();
     }
-    if (warp == 5) tmem_alloc(holder, 512);
+    if (warp == 9) tmem_alloc(holder, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + 8 * 10);
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + 8 * 13);
 
-    if (warp == 4) {
+    if (warp == 8) {
         if (lane == 0) {
             mbar_expect_tx(b_kv, 2 * kTile);
             for (int blk = 0; blk < 2; ++blk) {
@@ -659,16 +795,17 @@ __global__ void __launch_bounds__(192, 1)
             }
             bool ok = true;
             for (int n = 0; n < G && ok; ++n) {
-                if (n > 0) ok = mbar_wait(b_qe, (n - 1) & 1, status, 100);
+                const int b = n & 1, u = n >> 1;
+                if (u > 0) ok = mbar_wait(b_qe(b), (u - 1) & 1, status, 100);
                 if (!ok) break;
-                mbar_expect_tx(b_qf, 2 * kTile);
+                mbar_expect_tx(b_qf(b), 2 * kTile);
                 for (int blk = 0; blk < 2; ++blk) {
-                    tma_load_3d(qa + blk * 16384, &tm_q, blk * 64, g * G + n, off, b_qf);
-                    tma_load_3d(da + blk * 16384, &tm_do, blk * 64, g * G + n, off, b_qf);
+                    tma_load_3d(qa(b) + blk * 16384, &tm_q, blk * 64, g * G + n, off, b_qf(b));
+                    tma_load_3d(da(b) + blk * 16384, &tm_do, blk * 64, g * G + n, off, b_qf(b));
                 }
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         if (lane == 0) {
             constexpr uint32_t ID_KK = idesc_bf16(128, 128, false, false);   // B K-major
             constexpr uint32_t ID_KM = idesc_bf16(128, 128, false, true);    // B MN-major
@@ -692,33 +829,40 @@ __global__ void __launch_bounds__(192, 1)
                 mma_commit(b_inter);
             }
             for (int n = 0; n < G && ok; ++n) {
-                ok = mbar_wait(b_qf, n & 1, status, 103);
+                const int b = n & 1;
+                ok = mbar_wait(b_qf(b), (n >> 1) & 1, status, 103);
                 if (!ok) break;
                 tc_fence_after();
+                const uint32_t q_s = qa(b), do_s = da(b);
 #pragma unroll
                 for (int k = 0; k < kD / 16; ++k) {   // S^T = K Q^T
                     const uint32_t o = (k >> 2) * 16384 + (k & 3) * 32;
-                    mma_bf16_ss(tmem + 256, sdesc_sw128(ka + o, 16, 1024), sdesc_sw128(qa + o, 16, 1024), ID_KK,
+                    mma_bf16_ss(tmem + 256, sdesc_sw128(ka + o, 16, 1024), sdesc_sw128(q_s + o, 16, 1024), ID_KK,
                                 k > 0);
                 }
 #pragma unroll
                 for (int k = 0; k < kD / 16; ++k) {   // A^T = V dO^T
                     const uint32_t o = (k >> 2) * 16384 + (k & 3) * 32;
-                    mma_bf16_ss(tmem + 384, sdesc_sw128(va + o, 16, 1024), sdesc_sw128(da + o, 16, 1024), ID_KK,
+                    mma_bf16_ss(tmem + 384, sdesc_sw128(va + o, 16, 1024), sdesc_sw128(do_s + o, 16, 1024), ID_KK,
                                 k > 0);
                 }
                 mma_commit(b_sa);
-                ok = mbar_wait(b_pa, n & 1, status, 104);
-                if (ok && n == 0) ok = mbar_wait(b_scaled, 0, status, 105);   // carried-in rows scaled
+                for (int h = 0; h < 2 && ok; ++h) {
+                    ok = mbar_wait(b_pa(h), n & 1, status, 104);
+                    if (ok && n == 0 && h == 0) ok = mbar_wait(b_scaled, 0, status, 105);   // carried-in rows scaled
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int k = 4 * h; k < 4 * h + 4; ++k)   // dV += P^T dO (queries 16k .. 16k + 15,
+                        mma_bf16_ts(tmem + 128, tmem + 256 + h * 64 + (k & 3) * 8,   // packed at 64h + 8 (k % 4))
+                                    sdesc_sw128(do_s + k * 2048, 16384, 1024), ID_KM, 1u);
+#pragma unroll
+                    for (int k = 4 * h; k < 4 * h + 4; ++k)   // dK += dA^T Q
+                        mma_bf16_ts(tmem, tmem + 384 + h * 64 + (k & 3) * 8, sdesc_sw128(q_s + k * 2048, 16384, 1024),
+                                    ID_KM, 1u);
+                }
                 if (!ok) break;
-                tc_fence_after();
-#pragma unroll
-                for (int k = 0; k < kChunk / 16; ++k)   // dV += P^T dO
-                    mma_bf16_ts(tmem + 128, tmem + 256 + k * 8, sdesc_sw128(da + k * 2048, 16384, 1024), ID_KM, 1u);
-#pragma unroll
-                for (int k = 0; k < kChunk / 16; ++k)   // dK += dA^T Q
-                    mma_bf16_ts(tmem, tmem + 384 + k * 8, sdesc_sw128(qa + k * 2048, 16384, 1024), ID_KM, 1u);
-                mma_commit(b_qe);   // Q / dO slots and T1 / T2 free again
+                mma_commit(b_qe(b));   // slot b free again once these products have read it
             }
             if (ok) mma_commit(b_done);
             mma_commit(b_drain);
@@ -726,22 +870,14 @@ __global__ void __launch_bounds__(192, 1)
         }
         __syncwarp();
     } else {
-        const int m = threadIdx.x;   // key row m'; key feature when staging Rsum
-        const uint32_t lane_base = tmem + ((uint32_t)(warp << 5) << 16);
+        const int m = ((warp & 3) << 5) + lane;   // key row m'
+        const int hc = warp >> 2;                  // query half; dK (0) or dV (1)
+        const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) << 5) << 16);
         const float lg = log2f(decay[g]);
         // Rsum (fp32 [key feature][value feature]) -> bf16, laid out like a value tile
-        {
-            const float4* src = reinterpret_cast<const float4*>(rsum + (((size_t)chunk * hkv + g) * kD + m) * kD);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const float4 a4 = src[2 * j], b4 = src[2 * j + 1];
-                const int blk = j >> 3, cj = j & 7;
-                st_shared_v4(ra + blk * 16384 + sw128_offset(m, cj), pack_bf16x2(a4.x, a4.y),
-                             pack_bf16x2(a4.z, a4.w), pack_bf16x2(b4.x, b4.y), pack_bf16x2(b4.z, b4.w));
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(b_r);
-        }
+        stage_state_bf16<16>(rsum + ((size_t)chunk * hkv + g) * kD * kD, ra, warp, lane);
+        fence_proxy_async_smem();
+        mbar_arrive(b_r);
         bool ok = mbar_wait(b_inter, 0, status, 107);
         ok = __all_sync(0xffffffffu, ok);
         if (ok) {
@@ -749,29 +885,30 @@ __global__ void __launch_bounds__(192, 1)
             tc_fence_after();
             const float w = m < L ? exp2f((float)(L - 1 - m) * lg) : 0.f;
 #pragma unroll
-            for (int part = 0; part < 2; ++part)
+            for (int cc = 0; cc < 4; ++cc) {   // dK (half 0) or dV (half 1)
+                float v[32];
+                tmem_ld32(lane_base + hc * 128 + cc * 32, v);
+                tmem_wait_ld();
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    float v[32];
-                    tmem_ld32(lane_base + part * 128 + cc * 32, v);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int u = 0; u < 32; ++u) v[u] *= w;
-                    tmem_st32(lane_base + part * 128 + cc * 32, v);
-                }
+                for (int u = 0; u < 32; ++u) v[u] *= w;
+                tmem_st32(lane_base + hc * 128 + cc * 32, v);
+            }
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(b_scaled);
         }
+        const float* wt = wtab + 128 - m;   // wt[m] = scale * gamma^(m - m'), 0 for m < m'
         for (int n = 0; n < G; ++n) {
             if (ok) ok = mbar_wait(b_sa, n & 1, status, 108);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) continue;
             tc_fence_after();
             // P^T[m', m] = scale S^T gamma^(m-m'), dA^T[m', m] = scale A^T gamma^(m-m'),
-            // for m' <= m < L; packed bf16 over the first 64 columns of each region
+            // for m' <= m < L; this half's 64 queries packed as bf16 over the first
+            // 32 of its columns in each region
 #pragma unroll 2
-            for (int cc = 0; cc < 8; ++cc) {   // 16 columns at a time
+            for (int cq = 0; cq < 4; ++cq) {   // 16 columns at a time
+                const int cc = 4 * hc + cq;
                 float s[16], a[16];
                 tmem_ld16(lane_base + 256 + cc * 16, s);
                 tmem_ld16(lane_base + 384 + cc * 16, a);
@@ -780,41 +917,38 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                 for (int w2 = 0; w2 < 8; ++w2) {
                     const int c0 = cc * 16 + 2 * w2, c1 = c0 + 1;
-                    const float w0 = (m <= c0 && c0 < L) ? scale * exp2f((float)(c0 - m) * lg) : 0.f;
-                    const float w1 = (m <= c1 && c1 < L) ? scale * exp2f((float)(c1 - m) * lg) : 0.f;
+                    const float w0 = c0 < L ? wt[c0] : 0.f;
+                    const float w1 = c1 < L ? wt[c1] : 0.f;
                     pw[w2] = pack_bf16x2(s[2 * w2] * w0, s[2 * w2 + 1] * w1);
                     aw[w2] = pack_bf16x2(a[2 * w2] * w0, a[2 * w2 + 1] * w1);
                 }
                 // over columns this thread has already read
-                tmem_st8(lane_base + 256 + cc * 8, pw);
-                tmem_st8(lane_base + 384 + cc * 8, aw);
+                tmem_st8(lane_base + 256 + hc * 64 + cq * 8, pw);
+                tmem_st8(lane_base + 384 + hc * 64 + cq * 8, aw);
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(b_pa);
+            mbar_arrive(b_pa(hc));
         }
         if (ok) ok = mbar_wait(b_done, 0, status, 109);
         ok = __all_sync(0xffffffffu, ok);
         if (ok) {
             tc_fence_after();
+            uint4* dst = reinterpret_cast<uint4*>((hc ? dv : dk) + ((size_t)(off + m) * hkv + g) * kD);
 #pragma unroll
-            for (int part = 0; part < 2; ++part) {
-                uint4* dst = reinterpret_cast<uint4*>((part ? dv : dk) + ((size_t)(off + m) * hkv + g) * kD);
+            for (int cc = 0; cc < 4; ++cc) {
+                float v[32];
+                tmem_ld32(lane_base + hc * 128 + cc * 32, v);
+                tmem_wait_ld();
+                if (m < L) {
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    float v[32];
-                    tmem_ld32(lane_base + part * 128 + cc * 32, v);
-                    tmem_wait_ld();
-                    if (m < L) {
-#pragma unroll
-                        for (int w = 0; w < 4; ++w) {
-                            uint4 x;
-                            x.x = pack_bf16x2(v[8 * w], v[8 * w + 1]);
-                            x.y = pack_bf16x2(v[8 * w + 2], v[8 * w + 3]);
-                            x.z = pack_bf16x2(v[8 * w + 4], v[8 * w + 5]);
-                            x.w = pack_bf16x2(v[8 * w + 6], v[8 * w + 7]);
-                            dst[cc * 4 + w] = x;
-                        }
+                    for (int w = 0; w < 4; ++w) {
+                        uint4 x;
+                        x.x = pack_bf16x2(v[8 * w], v[8 * w + 1]);
+                        x.y = pack_bf16x2(v[8 * w + 2], v[8 * w + 3]);
+                        x.z = pack_bf16x2(v[8 * w + 4], v[8 * w + 5]);
+                        x.w = pack_bf16x2(v[8 * w + 6], v[8 * w + 7]);
+                        dst[cc * 4 + w] = x;
                     }
                 }
             }
@@ -822,7 +956,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -885,10 +1019,10 @@ int tree_attn_linear_fwd(tree_attn_plan_t P, const void* q, const void* k, const
         return TREE_ATTN_ERR_CUDA;
     lin_delta_kernel<<<(unsigned)(nc * hkv), 160, kDeltaSmem, s>>>(tk, tv, D->chunks, decay, hkv, ds, status);
     if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
-    lin_scan_kernel<<<dim3(kD * kD / 256, hkv), 256, 0, s>>>(D->lnodes, P->n_nodes, D->chunks, decay, hkv, ds, s_in,
+    lin_scan_kernel<<<dim3(kD * kD / 256, hkv), 256, 0, s>>>(D->lnodes, (int)nc, D->chunks, decay, hkv, ds, s_in,
                                                              s_out);
     if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
-    lin_out_kernel<<<(unsigned)(nc * hkv), 192, kOutSmem, s>>>(tq, tk, tv, D->chunks, decay, s_in,
+    lin_out_kernel<<<(unsigned)(nc * hkv), kLinThreads, kOutSmem, s>>>(tq, tk, tv, D->chunks, decay, s_in,
                                                               static_cast<uint16_t*>(o), hq, hkv, scale, status);
     return cudaGetLastError() == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
 }
@@ -932,18 +1066,18 @@ int tree_attn_linear_bwd(tree_attn_plan_t P, const void* q, const void* k, const
     // dQ: the forward with (q, k, v) = (dO, V, K)
     lin_delta_kernel<<<(unsigned)(nc * hkv), 160, kDeltaSmem, s>>>(tv, tk, D->chunks, decay, hkv, r0, status);
     if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
-    lin_scan_kernel<<<dim3(kD * kD / 256, hkv), 256, 0, s>>>(D->lnodes, P->n_nodes, D->chunks, decay, hkv, r0, r1, r2);
+    lin_scan_kernel<<<dim3(kD * kD / 256, hkv), 256, 0, s>>>(D->lnodes, (int)nc, D->chunks, decay, hkv, r0, r1, r2);
     if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
-    lin_out_kernel<<<(unsigned)(nc * hkv), 192, kOutSmem, s>>>(tdo, tv, tk, D->chunks, decay, r1,
+    lin_out_kernel<<<(unsigned)(nc * hkv), kLinThreads, kOutSmem, s>>>(tdo, tv, tk, D->chunks, decay, r1,
                                                               static_cast<uint16_t*>(dq), hq, hkv, scale, status);
     if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
     // dK, dV: adjoint increments, the reverse scan, then the per-chunk products
     lin_bwd_f_kernel<<<(unsigned)(nc * hkv), 160, kAdjSmem, s>>>(tq, tdo, D->chunks, decay, hq, hkv, scale, r0, status);
     if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
-    lin_bwd_scan_kernel<<<dim3(kD * kD / 256, hkv), 256, 0, s>>>(D->lnodes, P->n_nodes, D->chunks, decay, hkv, r0, r1,
+    lin_bwd_scan_kernel<<<dim3(kD * kD / 256, hkv), 256, 0, s>>>(D->lnodes, P->n_nodes, (int)nc, D->chunks, decay, hkv, r0, r1,
                                                                  r2);
     if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
-    lin_bwd_kv_kernel<<<(unsigned)(nc * hkv), 192, kKvSmem, s>>>(tq, tk, tv, tdo, D->chunks, decay, r1,
+    lin_bwd_kv_kernel<<<(unsigned)(nc * hkv), kLinThreads, kKvSmem, s>>>(tq, tk, tv, tdo, D->chunks, decay, r1,
                                                                  static_cast<uint16_t*>(dk), static_cast<uint16_t*>(dv),
                                                                  hq, hkv, scale, status);
     return cudaGetLastError() == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;

@@ -49,6 +49,9 @@ def check(t, hq, hkv, decay, seed):
     ([-1, 0, 0], [127, 129, 1], 4, 2, [0.95, 1.0]),            # chunk boundaries around 128
     ([-1, 0, 0, 1, 1, 2], [128, 200, 5, 64, 300, 33], 4, 1, [0.99]),
     ([-1, 0, 1, -1, 3], [70, 60, 5, 300, 2], 3, 3, [1.0, 0.9, 0.995]),   # forest, group 1
+    # a star: the children's first chunks fall in later batches of the scan than
+    # the root's last one
+    ([-1] + [0] * 20, [300] + [(17 * i) % 260 + 1 for i in range(20)], 4, 2, [0.99, 1.0]),
 ])
 def test_small_trees(parent, seg_len, hq, hkv, decay):
     check(WT.Tree("s", parent, seg_len), hq, hkv, decay, 11)
@@ -95,6 +98,7 @@ def check_bwd(t, hq, hkv, decay, seed):
     ([-1, 0, 0], [127, 129, 1], 4, 2, [0.95, 1.0]),
     ([-1, 0, 0, 1, 1, 2], [128, 200, 5, 64, 300, 33], 4, 1, [0.99]),
     ([-1, 0, 1, -1, 3], [70, 60, 5, 300, 2], 3, 3, [1.0, 0.9, 0.995]),
+    ([-1] + [0] * 20, [300] + [(17 * i) % 260 + 1 for i in range(20)], 4, 2, [0.99, 1.0]),   # star
 ])
 def test_bwd_small_trees(parent, seg_len, hq, hkv, decay):
     check_bwd(WT.Tree("s", parent, seg_len), hq, hkv, decay, 21)
@@ -105,6 +109,15 @@ def test_bwd_random_trees(seed):
     rng = np.random.default_rng(400 + seed)
     t = WT.random_tree(rng, int(rng.integers(3, 10)), [1, 17, 127, 128, 129, 255], n_roots=1 + seed % 2)
     check_bwd(t, 4, 2, [0.97, 1.0], 40 + seed)
+
+
+@pytest.mark.parametrize("seed", range(2))
+def test_many_nodes(seed):
+    # 40 to 60 short nodes: node boundaries at every position of the scans' batches
+    rng = np.random.default_rng(500 + seed)
+    t = WT.random_tree(rng, int(rng.integers(40, 61)), [1, 17, 129], n_roots=1 + seed)
+    check(t, 2, 1, [0.98], 60 + seed)
+    check_bwd(t, 2, 1, [0.98], 70 + seed)
 
 
 def test_bwd_timing_segment_tree():

@@ -230,8 +230,10 @@ int tree_attn_bwd_stages(tree_attn_plan_t plan, const void* q, const void* k, co
  *    4 bytes per token (rounded up to a multiple of 128 tokens), 4 per q-tile
  *    and 16 per backward work item, e.g. 45 KB for an 11k-token tree.  A copy
  *    from pageable memory is staged through the driver before the call returns,
- *    so the host waits for it.  The call makes no cudaMalloc, cudaFree or other
- *    allocating call.
+ *    so the host waits for it, and such a copy is not allowed during stream
+ *    capture: this call cannot be captured in a CUDA graph (capture
+ *    tree_attn_bwd with a workspace instead).  The call makes no cudaMalloc,
+ *    cudaFree or other allocating call.
  * Arguments, layouts, stream semantics and the other status codes are those of
  * tree_attn_bwd. */
 int tree_attn_bwd_noalloc(tree_attn_plan_t plan, const void* q, const void* k, const void* v,

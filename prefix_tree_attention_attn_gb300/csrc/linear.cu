@@ -7,15 +7,17 @@
 //                     the tensor core (M = 128 key features, N = 128 value
 //                     features, K = the chunk's tokens), read out of TMEM to
 //                     an fp32 workspace;
-//   lin_scan_kernel   per state entry (d x d x hkv threads): walks the nodes in
-//                     packed order, the entering state of each chunk
-//                     S_in = gamma^L S_in(prev) + dS(prev), a child starting
-//                     from its parent's exit state -- the branch-point handoff;
+//   lin_scan_kernel   per state entry (d x d x hkv threads): walks the chunks
+//                     in packed order, the entering state of each chunk
+//                     S_in = gamma^L S_in(prev) + dS(prev) in fp32, a node's
+//                     first chunk starting from its parent's exit state -- the
+//                     branch-point handoff; S_in leaves as bf16, the operand
+//                     precision of the next kernel;
 //   lin_out_kernel    per (chunk, kv-head), the group's q-heads in turn:
-//                     S = Q K^T, O = Q S_in (bf16 copy of the state as the B
-//                     operand), then P = S o decay mask (registers, written
-//                     back over S as packed bf16), O rows scaled by
-//                     gamma^(m+1), O += P V; O out as bf16.
+//                     S = Q K^T, O = Q S_in (S_in TMA-loaded like a value
+//                     tile), then P = S o decay mask (registers, written back
+//                     over S as packed bf16), O rows scaled by gamma^(m+1),
+//                     O += P V; O out as bf16.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -35,10 +37,6 @@ namespace {
 constexpr int kChunk = 128;
 constexpr int kD = 128;
 constexpr int kTile = kChunk * kD * 2;   // 32 KB bf16 tile
-
-__device__ __forceinline__ void st_shared_v2_b32(uint32_t addr, uint32_t a, uint32_t b) {
-    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
-}
 
 __device__ __forceinline__ void bulk_store_s2g(void* dst, uint32_t src, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
@@ -80,24 +78,16 @@ __device__ __forceinline__ void store_rows_f32(uint32_t tmem_rows, uint32_t stag
     __syncwarp();
 }
 
-// An fp32 d x d state (row = key feature, fp32 [key feature][value feature])
-// -> a bf16 tile at `dst` laid out like a value tile (two 64-column
-// 128B-swizzled blocks).  Warps 0 .. kRows/128-1 take kRows rows each and read
-// one row per instruction (512 contiguous bytes, lane l holding features
-// 4l .. 4l+3), so every global load is fully used; lane l then writes its 8
-// bytes into the 16-byte piece ((l & 15) >> 1) of block (l >> 4), two
-// wavefronts per row.
-template <int kRows>
-__device__ __forceinline__ void stage_state_bf16(const float* __restrict__ state, uint32_t dst, int warp, int lane) {
-    const float4* src = reinterpret_cast<const float4*>(state);
-    const uint32_t blk = lane >> 4, cj = (lane & 15) >> 1, half = lane & 1;
-#pragma unroll 16
-    for (int rr = 0; rr < kRows; ++rr) {   // 16 rows' loads in flight
-        const int row = warp * kRows + rr;
-        const float4 a4 = src[row * 32 + lane];
-        st_shared_v2_b32(dst + blk * 16384 + sw128_offset(row, cj) + half * 8, pack_bf16x2(a4.x, a4.y),
-                         pack_bf16x2(a4.z, a4.w));
-    }
+// The scans hand each chunk's d x d state to the tensor-core kernels as bf16,
+// laid out [chunk][row][kv-head][col] (row = key feature), i.e. as a token-major
+// [chunks * 128, hkv, 128] tensor that the kernels TMA-load like a value tile.
+__device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(f);   // round to nearest even, as pack_bf16x2
+    return *reinterpret_cast<const uint16_t*>(&h);
+}
+
+__device__ __forceinline__ size_t state16_index(int chunk, int e, int g, int hkv) {
+    return (((size_t)chunk * kChunk + (e >> 7)) * hkv + g) * kD + (e & 127);
 }
 
 // ---- dS per (chunk, kv-head) -------------------------------------------------
@@ -210,7 +200,7 @@ constexpr int kScanWin = 1024;
 __global__ void __launch_bounds__(256) lin_scan_kernel(const int32_t* __restrict__ lnodes, int n_chunks,
                                                      const int32_t* __restrict__ chunks,
                                                      const float* __restrict__ decay, int hkv,
-                                                     const float* __restrict__ ds, float* __restrict__ s_in,
+                                                     const float* __restrict__ ds, uint16_t* __restrict__ s_in16,
                                                      float* __restrict__ s_out) {
     __shared__ int w_len[kScanWin], w_node[kScanWin];
     const int e = blockIdx.x * blockDim.x + threadIdx.x;   // state entry (row * d + col)
@@ -243,7 +233,7 @@ __global__ void __launch_bounds__(256) lin_scan_kernel(const int32_t* __restrict
                         if (par != cur) S = par < 0 ? 0.f : s_out[((size_t)par * hkv + g) * dd + e];
                         cur = node;
                     }
-                    s_in[((size_t)(w0 + c + u) * hkv + g) * dd + e] = S;
+                    s_in16[state16_index(w0 + c + u, e, g, hkv)] = float_to_bf16_bits(S);
                     S = exp2f((float)w_len[c + u] * lg) * S + dsv[u];
                 }
         }
@@ -269,8 +259,8 @@ constexpr int kLinThreads = 32 * kLinWarps;
 
 __global__ void __launch_bounds__(kLinThreads, 1)
     lin_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const int32_t* __restrict__ chunks,
-                   const float* __restrict__ decay, const float* __restrict__ s_in, uint16_t* __restrict__ out,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_s,
+                   const int32_t* __restrict__ chunks, const float* __restrict__ decay, uint16_t* __restrict__ out,
                    int hq, int hkv, float scale, int* status) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sb = smem_u32(smem);
@@ -282,9 +272,9 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     const int G = hq / hkv;
     const int chunk = blockIdx.x / hkv, g = blockIdx.x % hkv;
     const int off = chunks[4 * chunk], L = chunks[4 * chunk + 1];
-    // barriers: kv, sin, then per buffer b: qfull, qempty, sfull, o1, p, o2, oempty
+    // barriers: K, V and S_in, then per buffer b: qfull, qempty, sfull, o1, p, o2, oempty
     auto bar = [&](int i) { return sb + 8u * (uint32_t)i; };
-    const uint32_t b_kv = bar(0), b_sin = bar(1);
+    const uint32_t b_kv = bar(0);
     auto b_qf = [&](int b) { return bar(2 + b); };
     auto b_qe = [&](int b) { return bar(4 + b); };
     auto b_sf = [&](int b) { return bar(6 + b); };
@@ -302,7 +292,6 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     }
     if (threadIdx.x == 0) {
         mbar_init(b_kv, 1);
-        mbar_init(b_sin, 256);
         for (int b = 0; b < 2; ++b) {
             mbar_init(b_qf(b), 1);
             mbar_init(b_qe(b), 1);
@@ -323,10 +312,11 @@ __global__ void __launch_bounds__(kLinThreads, 1)
 
     if (warp == 8) {
         if (lane == 0) {
-            mbar_expect_tx(b_kv, 2 * kTile);
+            mbar_expect_tx(b_kv, 3 * kTile);
             for (int blk = 0; blk < 2; ++blk) {
                 tma_load_3d(ka + blk * 16384, &tm_k, blk * 64, g, off, b_kv);
                 tma_load_3d(va + blk * 16384, &tm_v, blk * 64, g, off, b_kv);
+                tma_load_3d(sina + blk * 16384, &tm_s, blk * 64, g, chunk * kChunk, b_kv);
             }
             bool ok = true;
             for (int n = 0; n < G && ok; ++n) {
@@ -343,7 +333,6 @@ __global__ void __launch_bounds__(kLinThreads, 1)
             constexpr uint32_t ID_S = idesc_bf16(128, 128, false, false);   // Q K^T
             constexpr uint32_t ID_O = idesc_bf16(128, 128, false, true);    // Q S_in, P V
             bool ok = mbar_wait(b_kv, 0, status, 83);
-            if (ok) ok = mbar_wait(b_sin, 0, status, 84);
             auto issue_pv = [&](int n) {
                 const int b = n & 1;
                 tc_fence_after();
@@ -394,11 +383,6 @@ __global__ void __launch_bounds__(kLinThreads, 1)
         const int col0 = (warp >> 2) * 64;         // this warp's 64 columns of S and of O
         const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) << 5) << 16);
         const float lg = log2f(decay[g]);
-        // S_in (fp32, [key feature][value feature]) -> bf16 B operand, laid out
-        // like a value tile: row = key feature, two 64-column 128B-swizzled blocks
-        stage_state_bf16<16>(s_in + ((size_t)chunk * hkv + g) * kD * kD, sina, warp, lane);
-        fence_proxy_async_smem();
-        mbar_arrive(b_sin);
         const float fo = scale * exp2f((float)(m + 1) * lg);   // weight of the carried-in part
         bool ok = true;
         for (int n = 0; n < G; ++n) {
@@ -672,13 +656,14 @@ __global__ void __launch_bounds__(160, 1)
 // packed order, so walking the chunks backwards every child's entering adjoint
 // has been added into its parent's slot (csum) before the parent's last chunk
 // is reached.  kBwdScanBatch adjoint increments are loaded at a time, as in the
-// forward scan (a smaller batch here measured faster than the forward's).
+// forward scan (a smaller batch here measured faster than the forward's).  The
+// sums run in fp32; Rsum leaves as bf16, the dK/dV kernel's operand precision.
 constexpr int kBwdScanBatch = 8;
 
 __global__ void __launch_bounds__(256) lin_bwd_scan_kernel(const int32_t* __restrict__ lnodes, int n_nodes,
                                                          int n_chunks, const int32_t* __restrict__ chunks,
                                                          const float* __restrict__ decay, int hkv,
-                                                         const float* __restrict__ f_in, float* __restrict__ rsum,
+                                                         const float* __restrict__ f_in, uint16_t* __restrict__ rsum16,
                                                          float* __restrict__ csum) {
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
     const int g = blockIdx.y;
@@ -708,7 +693,7 @@ __global__ void __launch_bounds__(256) lin_bwd_scan_kernel(const int32_t* __rest
                     cur = node[u];
                     acc = csum[((size_t)cur * hkv + g) * dd + e];
                 }
-                rsum[((size_t)(c - u) * hkv + g) * dd + e] = acc;
+                rsum16[state16_index(c - u, e, g, hkv)] = float_to_bf16_bits(acc);
                 acc = fv[u] + exp2f((float)len[u] * lg) * acc;
             }
     }
@@ -737,8 +722,8 @@ constexpr int kKvSmem = 2048 + 7 * kTile;   // barriers, mask table, K, V, Rsum 
 __global__ void __launch_bounds__(kLinThreads, 1)
     lin_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                      const int32_t* __restrict__ chunks, const float* __restrict__ decay,
-                      const float* __restrict__ rsum, uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, int hq,
+                      const __grid_constant__ CUtensorMap tm_r, const int32_t* __restrict__ chunks,
+                      const float* __restrict__ decay, uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, int hq,
                       int hkv, float scale, int* status) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sb = smem_u32(smem);
@@ -751,7 +736,7 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     const int chunk = blockIdx.x / hkv, g = blockIdx.x % hkv;
     const int off = chunks[4 * chunk], L = chunks[4 * chunk + 1];
     auto bar = [&](int i) { return sb + 8u * (uint32_t)i; };
-    const uint32_t b_kv = bar(0), b_r = bar(1), b_inter = bar(2), b_scaled = bar(3), b_sa = bar(8), b_done = bar(11),
+    const uint32_t b_kv = bar(0), b_inter = bar(2), b_scaled = bar(3), b_sa = bar(8), b_done = bar(11),
                    b_drain = bar(12), holder = bar(13);
     auto b_qf = [&](int b) { return bar(4 + b); };   // slot b's Q and dO have arrived
     auto b_qe = [&](int b) { return bar(6 + b); };   // slot b's Q and dO have been read
@@ -767,7 +752,6 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     }
     if (threadIdx.x == 0) {
         mbar_init(b_kv, 1);
-        mbar_init(b_r, 256);
         mbar_init(b_inter, 1);
         mbar_init(b_scaled, 256);
         for (int b = 0; b < 2; ++b) {
@@ -788,10 +772,11 @@ __global__ void __launch_bounds__(kLinThreads, 1)
 
     if (warp == 8) {
         if (lane == 0) {
-            mbar_expect_tx(b_kv, 2 * kTile);
+            mbar_expect_tx(b_kv, 3 * kTile);
             for (int blk = 0; blk < 2; ++blk) {
                 tma_load_3d(ka + blk * 16384, &tm_k, blk * 64, g, off, b_kv);
                 tma_load_3d(va + blk * 16384, &tm_v, blk * 64, g, off, b_kv);
+                tma_load_3d(ra + blk * 16384, &tm_r, blk * 64, g, chunk * kChunk, b_kv);
             }
             bool ok = true;
             for (int n = 0; n < G && ok; ++n) {
@@ -810,7 +795,6 @@ __global__ void __launch_bounds__(kLinThreads, 1)
             constexpr uint32_t ID_KK = idesc_bf16(128, 128, false, false);   // B K-major
             constexpr uint32_t ID_KM = idesc_bf16(128, 128, false, true);    // B MN-major
             bool ok = mbar_wait(b_kv, 0, status, 101);
-            if (ok) ok = mbar_wait(b_r, 0, status, 102);
             if (ok) {
                 tc_fence_after();
                 // carried-in parts: dK = V Rsum^T (Rsum rows = key features, i.e. K-major
@@ -874,10 +858,6 @@ __global__ void __launch_bounds__(kLinThreads, 1)
         const int hc = warp >> 2;                  // query half; dK (0) or dV (1)
         const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) << 5) << 16);
         const float lg = log2f(decay[g]);
-        // Rsum (fp32 [key feature][value feature]) -> bf16, laid out like a value tile
-        stage_state_bf16<16>(rsum + ((size_t)chunk * hkv + g) * kD * kD, ra, warp, lane);
-        fence_proxy_async_smem();
-        mbar_arrive(b_r);
         bool ok = mbar_wait(b_inter, 0, status, 107);
         ok = __all_sync(0xffffffffu, ok);
         if (ok) {
@@ -1011,7 +991,9 @@ int tree_attn_linear_fwd(tree_attn_plan_t P, const void* q, const void* k, const
     if ((st = get_status_ptr(dev, &status))) return st;
     char* ws = static_cast<char*>(workspace);
     float* ds = reinterpret_cast<float*>(ws + w.ds);
-    float* s_in = reinterpret_cast<float*>(ws + w.s_in);
+    uint16_t* s_in16 = reinterpret_cast<uint16_t*>(ws + w.s_in);   // bf16 entering states
+    CUtensorMap ts;
+    if ((st = make_tensor_map(&ts, s_in16, nc * kChunk, hkv, kD))) return st;
     float* s_out = reinterpret_cast<float*>(ws + w.s_out);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaFuncSetAttribute(lin_delta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDeltaSmem) != cudaSuccess ||
@@ -1019,10 +1001,10 @@ int tree_attn_linear_fwd(tree_attn_plan_t P, const void* q, const void* k, const
         return TREE_ATTN_ERR_CUDA;
     lin_delta_kernel<<<(unsigned)(nc * hkv), 160, kDeltaSmem, s>>>(tk, tv, D->chunks, decay, hkv, ds, status);
     if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
-    lin_scan_kernel<<<dim3(kD * kD / 256, hkv), 256, 0, s>>>(D->lnodes, (int)nc, D->chunks, decay, hkv, ds, s_in,
+    lin_scan_kernel<<<dim3(kD * kD / 256, hkv), 256, 0, s>>>(D->lnodes, (int)nc, D->chunks, decay, hkv, ds, s_in16,
                                                              s_out);
     if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
-    lin_out_kernel<<<(unsigned)(nc * hkv), kLinThreads, kOutSmem, s>>>(tq, tk, tv, D->chunks, decay, s_in,
+    lin_out_kernel<<<(unsigned)(nc * hkv), kLinThreads, kOutSmem, s>>>(tq, tk, tv, ts, D->chunks, decay,
                                                               static_cast<uint16_t*>(o), hq, hkv, scale, status);
     return cudaGetLastError() == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
 }
@@ -1055,7 +1037,9 @@ int tree_attn_linear_bwd(tree_attn_plan_t P, const void* q, const void* k, const
     if ((st = get_status_ptr(dev, &status))) return st;
     char* ws = static_cast<char*>(workspace);
     float* r0 = reinterpret_cast<float*>(ws + w.ds);      // dS', then F
-    float* r1 = reinterpret_cast<float*>(ws + w.s_in);    // S'_in, then Rsum
+    uint16_t* r1 = reinterpret_cast<uint16_t*>(ws + w.s_in);   // bf16 S'_in, then bf16 Rsum
+    CUtensorMap tr1;
+    if ((st = make_tensor_map(&tr1, r1, nc * kChunk, hkv, kD))) return st;
     float* r2 = reinterpret_cast<float*>(ws + w.s_out);   // S'_out, then the per-node child sums
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaFuncSetAttribute(lin_delta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDeltaSmem) != cudaSuccess ||
@@ -1068,7 +1052,7 @@ int tree_attn_linear_bwd(tree_attn_plan_t P, const void* q, const void* k, const
     if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
     lin_scan_kernel<<<dim3(kD * kD / 256, hkv), 256, 0, s>>>(D->lnodes, (int)nc, D->chunks, decay, hkv, r0, r1, r2);
     if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
-    lin_out_kernel<<<(unsigned)(nc * hkv), kLinThreads, kOutSmem, s>>>(tdo, tv, tk, D->chunks, decay, r1,
+    lin_out_kernel<<<(unsigned)(nc * hkv), kLinThreads, kOutSmem, s>>>(tdo, tv, tk, tr1, D->chunks, decay,
                                                               static_cast<uint16_t*>(dq), hq, hkv, scale, status);
     if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
     // dK, dV: adjoint increments, the reverse scan, then the per-chunk products
@@ -1077,7 +1061,7 @@ int tree_attn_linear_bwd(tree_attn_plan_t P, const void* q, const void* k, const
     lin_bwd_scan_kernel<<<dim3(kD * kD / 256, hkv), 256, 0, s>>>(D->lnodes, P->n_nodes, (int)nc, D->chunks, decay, hkv, r0, r1,
                                                                  r2);
     if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
-    lin_bwd_kv_kernel<<<(unsigned)(nc * hkv), kLinThreads, kKvSmem, s>>>(tq, tk, tv, tdo, D->chunks, decay, r1,
+    lin_bwd_kv_kernel<<<(unsigned)(nc * hkv), kLinThreads, kKvSmem, s>>>(tq, tk, tv, tdo, tr1, D->chunks, decay,
                                                                  static_cast<uint16_t*>(dk), static_cast<uint16_t*>(dv),
                                                                  hq, hkv, scale, status);
     return cudaGetLastError() == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;

@@ -38,6 +38,12 @@ SMALL = [
     ([-1, 0, 0, 1, 1], [128, 128, 255, 1, 129], 8, 2, 128),  # group 4
     ([-1, 0, 1, -1, 3], [70, 60, 5, 300, 2], 3, 3, 64),      # forest, group 1 (odd)
     ([-1, 0, 0, 0, 0, 0], [256, 40, 1, 129, 300, 7], 6, 2, 64),  # group 3 (odd)
+    # caterpillar: a spine of 150 one-token nodes, each with a one-token leaf,
+    # so every tile is partial and the visible keys change from row to row
+    ([-1] + [2 * ((k - 1) // 2) for k in range(1, 300)], [1] * 300, 4, 2, 128),
+    # wide star: a 5-token root and 300 one-token leaves (each row sees the root
+    # and itself only)
+    ([-1] + [0] * 300, [5] + [1] * 300, 2, 1, 64),
 ]
 
 

@@ -242,10 +242,15 @@ __global__ void __launch_bounds__(256) lin_scan_kernel(const int32_t* __restrict
 }
 
 // ---- outputs per (chunk, kv-head): the group's q-heads one after another ------
-// K, V and the bf16 copy of S_in are loaded once for the G q-heads of the
-// group; Q comes through two slots and TMEM holds two heads (S / P at
-// [256b, 256b + 128), O at [256b + 128, 256b + 256) for buffer b = head & 1), so
-// one head's P and output overlap the next head's S and Q S_in products.
+// Persistent: a CTA keeps one kv-head g and walks the chunks j0, j0 + lanes,
+// j0 + 2 lanes, ... (grid = lanes x hkv, about one CTA per SM); every
+// (chunk, q-head) pair it meets is one "unit" u.  K, V and the bf16 copy of
+// S_in are loaded once per chunk for the G q-heads of the group; Q comes
+// through two slots and TMEM holds two units (S / P at [256b, 256b + 128), O at
+// [256b + 128, 256b + 256) for buffer b = u & 1), so one unit's P and output
+// overlap the next unit's S and Q S_in products -- across chunk boundaries too:
+// the next chunk's K and S_in load as soon as the last q-head's S and Q S_in
+// products have read them, and its V once the last P V product has read V.
 // warps 0-7: query row m = 32 (w % 4) + lane (the TMEM lanes warp w may
 // access), columns [64 (w / 4), 64 (w / 4) + 64) of S and of O -- two warps per
 // row, so that each SM sub-partition has two warps of element-wise work; P of
@@ -260,8 +265,8 @@ constexpr int kLinThreads = 32 * kLinWarps;
 __global__ void __launch_bounds__(kLinThreads, 1)
     lin_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_s,
-                   const int32_t* __restrict__ chunks, const float* __restrict__ decay, uint16_t* __restrict__ out,
-                   int hq, int hkv, float scale, int* status) {
+                   const int32_t* __restrict__ chunks, int n_chunks, int lanes, const float* __restrict__ decay,
+                   uint16_t* __restrict__ out, int hq, int hkv, float scale, int* status) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sb = smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -270,11 +275,15 @@ __global__ void __launch_bounds__(kLinThreads, 1)
         return;
     }
     const int G = hq / hkv;
-    const int chunk = blockIdx.x / hkv, g = blockIdx.x % hkv;
-    const int off = chunks[4 * chunk], L = chunks[4 * chunk + 1];
-    // barriers: K, V and S_in, then per buffer b: qfull, qempty, sfull, o1, p, o2, oempty
+    const int j0 = blockIdx.x / hkv, g = blockIdx.x % hkv;
+    if (j0 >= n_chunks) return;   // uniform: nothing set up yet
+    const int n_items = (n_chunks - 1 - j0) / lanes + 1;   // chunks j0 + i lanes < n_chunks
+    const int U = n_items * G;                              // units of this CTA
+    auto chunk_of = [&](int i) { return j0 + i * lanes; };
+    // barriers: K and S_in, V, their free signals, then per buffer b: qfull,
+    // qempty, sfull, o1, p, o2, oempty
     auto bar = [&](int i) { return sb + 8u * (uint32_t)i; };
-    const uint32_t b_kv = bar(0);
+    const uint32_t b_ks = bar(0), b_v = bar(1), b_kfree = bar(18), b_vfree = bar(19);
     auto b_qf = [&](int b) { return bar(2 + b); };
     auto b_qe = [&](int b) { return bar(4 + b); };
     auto b_sf = [&](int b) { return bar(6 + b); };
@@ -291,7 +300,10 @@ __global__ void __launch_bounds__(kLinThreads, 1)
         mtab[128 + threadIdx.x] = exp2f((float)threadIdx.x * log2f(decay[g]));
     }
     if (threadIdx.x == 0) {
-        mbar_init(b_kv, 1);
+        mbar_init(b_ks, 1);
+        mbar_init(b_v, 1);
+        mbar_init(b_kfree, 1);
+        mbar_init(b_vfree, 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(b_qf(b), 1);
             mbar_init(b_qe(b), 1);
@@ -312,40 +324,58 @@ __global__ void __launch_bounds__(kLinThreads, 1)
 
     if (warp == 8) {
         if (lane == 0) {
-            mbar_expect_tx(b_kv, 3 * kTile);
-            for (int blk = 0; blk < 2; ++blk) {
-                tma_load_3d(ka + blk * 16384, &tm_k, blk * 64, g, off, b_kv);
-                tma_load_3d(va + blk * 16384, &tm_v, blk * 64, g, off, b_kv);
-                tma_load_3d(sina + blk * 16384, &tm_s, blk * 64, g, chunk * kChunk, b_kv);
-            }
             bool ok = true;
-            for (int n = 0; n < G && ok; ++n) {
-                const int b = n & 1, u = n >> 1;
-                if (u > 0) ok = mbar_wait(b_qe(b), (u - 1) & 1, status, 89);
+            for (int i = 0; i < n_items && ok; ++i) {
+                const int chunk = chunk_of(i), off = chunks[4 * chunk];
+                // K and S_in: once the previous chunk's last S and Q S_in products read them
+                if (i > 0) ok = mbar_wait(b_kfree, (i - 1) & 1, status, 94);
                 if (!ok) break;
-                mbar_expect_tx(b_qf(b), kTile);
-                for (int blk = 0; blk < 2; ++blk)
-                    tma_load_3d(qa0 + b * kTile + blk * 16384, &tm_q, blk * 64, g * G + n, off, b_qf(b));
+                mbar_expect_tx(b_ks, 2 * kTile);
+                for (int blk = 0; blk < 2; ++blk) {
+                    tma_load_3d(ka + blk * 16384, &tm_k, blk * 64, g, off, b_ks);
+                    tma_load_3d(sina + blk * 16384, &tm_s, blk * 64, g, chunk * kChunk, b_ks);
+                }
+                for (int n = 0; n < G && ok; ++n) {
+                    const int u = i * G + n, b = u & 1, w = u >> 1;
+                    if (w > 0) ok = mbar_wait(b_qe(b), (w - 1) & 1, status, 89);
+                    if (!ok) break;
+                    mbar_expect_tx(b_qf(b), kTile);
+                    for (int blk = 0; blk < 2; ++blk)
+                        tma_load_3d(qa0 + b * kTile + blk * 16384, &tm_q, blk * 64, g * G + n, off, b_qf(b));
+                    // V after the second q-head's Q (the first with one q-head): the
+                    // previous chunk's last P V product, which must have read V, is
+                    // issued before this chunk's second S product
+                    if (n == (G > 1 ? 1 : 0)) {
+                        if (i > 0) ok = mbar_wait(b_vfree, (i - 1) & 1, status, 95);
+                        if (!ok) break;
+                        mbar_expect_tx(b_v, kTile);
+                        for (int blk = 0; blk < 2; ++blk) tma_load_3d(va + blk * 16384, &tm_v, blk * 64, g, off, b_v);
+                    }
+                }
             }
         }
     } else if (warp == 9) {
         if (lane == 0) {
             constexpr uint32_t ID_S = idesc_bf16(128, 128, false, false);   // Q K^T
             constexpr uint32_t ID_O = idesc_bf16(128, 128, false, true);    // Q S_in, P V
-            bool ok = mbar_wait(b_kv, 0, status, 83);
-            auto issue_pv = [&](int n) {
-                const int b = n & 1;
+            bool ok = true;
+            auto issue_pv = [&](int u) {
+                const int b = u & 1, i = u / G, n = u % G;
+                if (n == 0) ok = mbar_wait(b_v, i & 1, status, 96);   // this chunk's V
+                if (!ok) return;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < kChunk / 16; ++k)   // keys 16k .. 16k + 15 packed at 64 (k / 4) + 8 (k % 4)
                     mma_bf16_ts(tmem + 256 * b + 128, tmem + 256 * b + (k >> 2) * 64 + (k & 3) * 8,
                                 sdesc_sw128(va + k * 2048, 16384, 1024), ID_O, 1u);
                 mma_commit(b_o2(b));
+                if (n == G - 1) mma_commit(b_vfree);   // V read by the chunk's last P V
             };
-            for (int n = 0; n < G && ok; ++n) {
-                const int b = n & 1, u = n >> 1;
-                if (u > 0) ok = mbar_wait(b_oe(b), (u - 1) & 1, status, 90);   // buffer b read out
-                if (ok) ok = mbar_wait(b_qf(b), u & 1, status, 91);
+            for (int u = 0; u < U && ok; ++u) {
+                const int b = u & 1, w = u >> 1, i = u / G, n = u % G;
+                if (w > 0) ok = mbar_wait(b_oe(b), (w - 1) & 1, status, 90);   // buffer b read out
+                if (ok) ok = mbar_wait(b_qf(b), w & 1, status, 91);
+                if (ok && n == 0) ok = mbar_wait(b_ks, i & 1, status, 83);   // this chunk's K and S_in
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t qa = qa0 + b * kTile;
@@ -363,38 +393,40 @@ __global__ void __launch_bounds__(kLinThreads, 1)
                                 sdesc_sw128(sina + k * 2048, 16384, 1024), ID_O, k > 0);
                 }
                 mma_commit(b_o1(b));
-                mma_commit(b_qe(b));   // Q slot b is no longer read
-                if (n > 0) {           // the previous head's P V
-                    ok = mbar_wait(b_p((n - 1) & 1), ((n - 1) >> 1) & 1, status, 85);
+                mma_commit(b_qe(b));                       // Q slot b is no longer read
+                if (n == G - 1) mma_commit(b_kfree);       // K and S_in read by the chunk's last products
+                if (u > 0) {                               // the previous unit's P V
+                    ok = mbar_wait(b_p((u - 1) & 1), ((u - 1) >> 1) & 1, status, 85);
                     if (!ok) break;
-                    issue_pv(n - 1);
+                    issue_pv(u - 1);
                 }
             }
             if (ok) {
-                ok = mbar_wait(b_p((G - 1) & 1), ((G - 1) >> 1) & 1, status, 92);
-                if (ok) issue_pv(G - 1);
+                ok = mbar_wait(b_p((U - 1) & 1), ((U - 1) >> 1) & 1, status, 92);
+                if (ok) issue_pv(U - 1);
             }
             mma_commit(b_drain);
             mbar_wait(b_drain, 0, status, 93);
         }
         __syncwarp();
     } else {
-        const int m = ((warp & 3) << 5) + lane;   // query row; key feature when staging the state
+        const int m = ((warp & 3) << 5) + lane;   // query row
         const int col0 = (warp >> 2) * 64;         // this warp's 64 columns of S and of O
         const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) << 5) << 16);
         const float lg = log2f(decay[g]);
         const float fo = scale * exp2f((float)(m + 1) * lg);   // weight of the carried-in part
+        const float* wt = mtab + 128 + m;   // wt[-m'] = gamma^(m - m'), 0 past the diagonal
         bool ok = true;
-        for (int n = 0; n < G; ++n) {
-            const int b = n & 1, u = n >> 1, h = g * G + n;
+        for (int u = 0; u < U; ++u) {
+            const int b = u & 1, w = u >> 1, i = u / G, n = u % G, h = g * G + n;
+            const int chunk = chunk_of(i), off = chunks[4 * chunk], L = chunks[4 * chunk + 1];
             const uint32_t tS = lane_base + 256 * b, tO = tS + 128;
-            if (ok) ok = mbar_wait(b_sf(b), u & 1, status, 86);
+            if (ok) ok = mbar_wait(b_sf(b), w & 1, status, 86);
             ok = __all_sync(0xffffffffu, ok);
             if (ok) {
                 tc_fence_after();
                 // P[m, m'] = scale * S[m, m'] * gamma^(m - m') for m' <= m (rows m >= L
                 // are never stored, and for m < L every m' <= m lies in the chunk)
-                const float* wt = mtab + 128 + m;   // wt[-m'] = gamma^(m - m'), 0 past the diagonal
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
                     float v[32];
@@ -402,14 +434,14 @@ __global__ void __launch_bounds__(kLinThreads, 1)
                     tmem_wait_ld();
                     uint32_t pw[16];
 #pragma unroll
-                    for (int w = 0; w < 16; ++w) {
-                        const int c0 = col0 + cc * 32 + 2 * w, c1 = c0 + 1;
-                        pw[w] = pack_bf16x2(scale * v[2 * w] * wt[-c0], scale * v[2 * w + 1] * wt[-c1]);
+                    for (int x = 0; x < 16; ++x) {
+                        const int c0 = col0 + cc * 32 + 2 * x, c1 = c0 + 1;
+                        pw[x] = pack_bf16x2(scale * v[2 * x] * wt[-c0], scale * v[2 * x + 1] * wt[-c1]);
                     }
                     tmem_st16(tS + col0 + cc * 16, pw);
                 }
                 tmem_wait_st();
-                ok = mbar_wait(b_o1(b), u & 1, status, 87);
+                ok = mbar_wait(b_o1(b), w & 1, status, 87);
             }
             ok = __all_sync(0xffffffffu, ok);
             if (ok) {
@@ -420,13 +452,13 @@ __global__ void __launch_bounds__(kLinThreads, 1)
                     tmem_ld32(tO + col0 + cc * 32, v);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int w = 0; w < 32; ++w) v[w] *= fo;
+                    for (int x = 0; x < 32; ++x) v[x] *= fo;
                     tmem_st32(tO + col0 + cc * 32, v);
                 }
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(b_p(b));
-                ok = mbar_wait(b_o2(b), u & 1, status, 88);
+                ok = mbar_wait(b_o2(b), w & 1, status, 88);
             }
             ok = __all_sync(0xffffffffu, ok);
             if (ok) {
@@ -439,18 +471,18 @@ __global__ void __launch_bounds__(kLinThreads, 1)
                     tmem_wait_ld();
                     if (m < L) {
 #pragma unroll
-                        for (int w = 0; w < 4; ++w) {
-                            uint4 x;
-                            x.x = pack_bf16x2(v[8 * w], v[8 * w + 1]);
-                            x.y = pack_bf16x2(v[8 * w + 2], v[8 * w + 3]);
-                            x.z = pack_bf16x2(v[8 * w + 4], v[8 * w + 5]);
-                            x.w = pack_bf16x2(v[8 * w + 6], v[8 * w + 7]);
-                            dst[cc * 4 + w] = x;
+                        for (int x = 0; x < 4; ++x) {
+                            uint4 y;
+                            y.x = pack_bf16x2(v[8 * x], v[8 * x + 1]);
+                            y.y = pack_bf16x2(v[8 * x + 2], v[8 * x + 3]);
+                            y.z = pack_bf16x2(v[8 * x + 4], v[8 * x + 5]);
+                            y.w = pack_bf16x2(v[8 * x + 6], v[8 * x + 7]);
+                            dst[cc * 4 + x] = y;
                         }
                     }
                 }
                 tc_fence_before();
-                mbar_arrive(b_oe(b));   // buffer b may take the head after next
+                mbar_arrive(b_oe(b));   // buffer b may take the unit after next
             }
         }
     }
@@ -944,6 +976,14 @@ __global__ void __launch_bounds__(kLinThreads, 1)
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// Chunk lanes of the persistent output kernel: about one CTA per SM in all
+// (lanes x hkv CTAs), at least one lane, at most one per chunk.
+int out_lanes(int dev, int64_t n_chunks, int hkv) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 1;
+    return (int)std::max<int64_t>(1, std::min<int64_t>(n_chunks, sms / hkv));
+}
+
 }  // namespace
 
 }  // namespace treeattn
@@ -1004,8 +1044,10 @@ int tree_attn_linear_fwd(tree_attn_plan_t P, const void* q, const void* k, const
     lin_scan_kernel<<<dim3(kD * kD / 256, hkv), 256, 0, s>>>(D->lnodes, (int)nc, D->chunks, decay, hkv, ds, s_in16,
                                                              s_out);
     if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
-    lin_out_kernel<<<(unsigned)(nc * hkv), kLinThreads, kOutSmem, s>>>(tq, tk, tv, ts, D->chunks, decay,
-                                                              static_cast<uint16_t*>(o), hq, hkv, scale, status);
+    const int lanes = out_lanes(dev, nc, hkv);
+    lin_out_kernel<<<(unsigned)(lanes * hkv), kLinThreads, kOutSmem, s>>>(tq, tk, tv, ts, D->chunks, (int)nc, lanes,
+                                                                      decay, static_cast<uint16_t*>(o), hq, hkv,
+                                                                      scale, status);
     return cudaGetLastError() == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
 }
 
@@ -1052,8 +1094,10 @@ int tree_attn_linear_bwd(tree_attn_plan_t P, const void* q, const void* k, const
     if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
     lin_scan_kernel<<<dim3(kD * kD / 256, hkv), 256, 0, s>>>(D->lnodes, (int)nc, D->chunks, decay, hkv, r0, r1, r2);
     if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
-    lin_out_kernel<<<(unsigned)(nc * hkv), kLinThreads, kOutSmem, s>>>(tdo, tv, tk, tr1, D->chunks, decay,
-                                                              static_cast<uint16_t*>(dq), hq, hkv, scale, status);
+    const int lanes = out_lanes(dev, nc, hkv);
+    lin_out_kernel<<<(unsigned)(lanes * hkv), kLinThreads, kOutSmem, s>>>(tdo, tv, tk, tr1, D->chunks, (int)nc, lanes,
+                                                                      decay, static_cast<uint16_t*>(dq), hq, hkv,
+                                                                      scale, status);
     if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
     // dK, dV: adjoint increments, the reverse scan, then the per-chunk products
     lin_bwd_f_kernel<<<(unsigned)(nc * hkv), 160, kAdjSmem, s>>>(tq, tdo, D->chunks, decay, hq, hkv, scale, r0, status);

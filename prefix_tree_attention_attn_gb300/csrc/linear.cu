@@ -736,27 +736,32 @@ __global__ void __launch_bounds__(256) lin_bwd_scan_kernel(const int32_t* __rest
 }
 
 // ---- dK, dV per (chunk, kv-head) ------------------------------------------------
+// Persistent like the output kernel: a CTA keeps kv-head g and walks chunks
+// j0, j0 + lanes, ...; unit u = one (chunk, q-head) pair.
 // TMEM: dK [0, 128), dV [128, 256), S^T -> P^T [256, 384), A^T -> dA^T [384, 512).
 // warps 0-7: key row m' = 32 (w % 4) + lane (the TMEM lanes warp w may access);
 // warp w < 4 takes queries [0, 64) of S^T and A^T (packed over their first 32
 // columns) and dK, warp w >= 4 queries [64, 128) (packed at [64, 96)) and dV;
-// warp 8: loads; warp 9: TMEM owner, lane 0 issues the MMAs.  The group's q-heads run
-// one after another through two Q / dO slot pairs, so the next head's tiles
-// arrive while the current head is worked on; its S^T and A^T products are
-// issued right after the current head's dV and dK products, which the tensor
+// warp 8: loads; warp 9: TMEM owner, lane 0 issues the MMAs.  The q-heads run
+// one after another through two Q / dO slot pairs, so the next unit's tiles
+// arrive while the current unit is worked on; its S^T and A^T products are
+// issued right after the current unit's dV and dK products, which the tensor
 // core completes first (products issued by one thread run in issue order), so
 // P^T and dA^T are read before they are overwritten.  The two query halves are
 // masked by different warps, and each half's dV and dK products start as soon
-// as that half is done.  The mask weight
-// scale * gamma^(m - m') depends on m - m' alone and is tabulated per CTA.
+// as that half is done.  At a chunk boundary the next chunk's K, V and Rsum
+// load once the last unit's S^T and A^T products have read them, and its first
+// S^T and A^T products run while the element-wise warps store the finished
+// chunk's dK and dV; its carried-in products wait for that store.  The mask
+// weight scale * gamma^(m - m') depends on m - m' alone and is tabulated per CTA.
 constexpr int kKvSmem = 2048 + 7 * kTile;   // barriers, mask table, K, V, Rsum (bf16), (Q, dO) x 2
 
 __global__ void __launch_bounds__(kLinThreads, 1)
     lin_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                      const __grid_constant__ CUtensorMap tm_r, const int32_t* __restrict__ chunks,
-                      const float* __restrict__ decay, uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, int hq,
-                      int hkv, float scale, int* status) {
+                      const __grid_constant__ CUtensorMap tm_r, const int32_t* __restrict__ chunks, int n_chunks,
+                      int lanes, const float* __restrict__ decay, uint16_t* __restrict__ dk,
+                      uint16_t* __restrict__ dv, int hq, int hkv, float scale, int* status) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sb = smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -765,11 +770,13 @@ __global__ void __launch_bounds__(kLinThreads, 1)
         return;
     }
     const int G = hq / hkv;
-    const int chunk = blockIdx.x / hkv, g = blockIdx.x % hkv;
-    const int off = chunks[4 * chunk], L = chunks[4 * chunk + 1];
+    const int j0 = blockIdx.x / hkv, g = blockIdx.x % hkv;
+    if (j0 >= n_chunks) return;   // uniform: nothing set up yet
+    const int n_items = (n_chunks - 1 - j0) / lanes + 1;
+    auto chunk_of = [&](int i) { return j0 + i * lanes; };
     auto bar = [&](int i) { return sb + 8u * (uint32_t)i; };
-    const uint32_t b_kv = bar(0), b_inter = bar(2), b_scaled = bar(3), b_sa = bar(8), b_done = bar(11),
-                   b_drain = bar(12), holder = bar(13);
+    const uint32_t b_kv = bar(0), b_kvfree = bar(1), b_inter = bar(2), b_scaled = bar(3), b_sa = bar(8),
+                   b_done = bar(11), b_drain = bar(12), holder = bar(13), b_dkvfree = bar(14);
     auto b_qf = [&](int b) { return bar(4 + b); };   // slot b's Q and dO have arrived
     auto b_qe = [&](int b) { return bar(6 + b); };   // slot b's Q and dO have been read
     auto b_pa = [&](int h) { return bar(9 + h); };   // query half h masked
@@ -784,6 +791,7 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     }
     if (threadIdx.x == 0) {
         mbar_init(b_kv, 1);
+        mbar_init(b_kvfree, 1);
         mbar_init(b_inter, 1);
         mbar_init(b_scaled, 256);
         for (int b = 0; b < 2; ++b) {
@@ -793,6 +801,7 @@ __global__ void __launch_bounds__(kLinThreads, 1)
         }
         mbar_init(b_sa, 1);
         mbar_init(b_done, 1);
+        mbar_init(b_dkvfree, 256);
         mbar_init(b_drain, 1);
         fence_mbar_init();
     }
@@ -804,21 +813,26 @@ __global__ void __launch_bounds__(kLinThreads, 1)
 
     if (warp == 8) {
         if (lane == 0) {
-            mbar_expect_tx(b_kv, 3 * kTile);
-            for (int blk = 0; blk < 2; ++blk) {
-                tma_load_3d(ka + blk * 16384, &tm_k, blk * 64, g, off, b_kv);
-                tma_load_3d(va + blk * 16384, &tm_v, blk * 64, g, off, b_kv);
-                tma_load_3d(ra + blk * 16384, &tm_r, blk * 64, g, chunk * kChunk, b_kv);
-            }
             bool ok = true;
-            for (int n = 0; n < G && ok; ++n) {
-                const int b = n & 1, u = n >> 1;
-                if (u > 0) ok = mbar_wait(b_qe(b), (u - 1) & 1, status, 100);
+            for (int i = 0; i < n_items && ok; ++i) {
+                const int chunk = chunk_of(i), off = chunks[4 * chunk];
+                if (i > 0) ok = mbar_wait(b_kvfree, (i - 1) & 1, status, 110);   // the previous chunk's done with them
                 if (!ok) break;
-                mbar_expect_tx(b_qf(b), 2 * kTile);
+                mbar_expect_tx(b_kv, 3 * kTile);
                 for (int blk = 0; blk < 2; ++blk) {
-                    tma_load_3d(qa(b) + blk * 16384, &tm_q, blk * 64, g * G + n, off, b_qf(b));
-                    tma_load_3d(da(b) + blk * 16384, &tm_do, blk * 64, g * G + n, off, b_qf(b));
+                    tma_load_3d(ka + blk * 16384, &tm_k, blk * 64, g, off, b_kv);
+                    tma_load_3d(va + blk * 16384, &tm_v, blk * 64, g, off, b_kv);
+                    tma_load_3d(ra + blk * 16384, &tm_r, blk * 64, g, chunk * kChunk, b_kv);
+                }
+                for (int n = 0; n < G && ok; ++n) {
+                    const int u = i * G + n, b = u & 1, w = u >> 1;
+                    if (w > 0) ok = mbar_wait(b_qe(b), (w - 1) & 1, status, 100);
+                    if (!ok) break;
+                    mbar_expect_tx(b_qf(b), 2 * kTile);
+                    for (int blk = 0; blk < 2; ++blk) {
+                        tma_load_3d(qa(b) + blk * 16384, &tm_q, blk * 64, g * G + n, off, b_qf(b));
+                        tma_load_3d(da(b) + blk * 16384, &tm_do, blk * 64, g * G + n, off, b_qf(b));
+                    }
                 }
             }
         }
@@ -826,61 +840,69 @@ __global__ void __launch_bounds__(kLinThreads, 1)
         if (lane == 0) {
             constexpr uint32_t ID_KK = idesc_bf16(128, 128, false, false);   // B K-major
             constexpr uint32_t ID_KM = idesc_bf16(128, 128, false, true);    // B MN-major
-            bool ok = mbar_wait(b_kv, 0, status, 101);
-            if (ok) {
-                tc_fence_after();
-                // carried-in parts: dK = V Rsum^T (Rsum rows = key features, i.e. K-major
-                // for this product), dV = K Rsum (the same tile read MN-major)
-#pragma unroll
-                for (int k = 0; k < kD / 16; ++k) {
-                    const uint32_t o = (k >> 2) * 16384 + (k & 3) * 32;
-                    mma_bf16_ss(tmem, sdesc_sw128(va + o, 16, 1024), sdesc_sw128(ra + o, 16, 1024), ID_KK, k > 0);
-                }
-#pragma unroll
-                for (int k = 0; k < kD / 16; ++k) {
-                    const uint32_t o = (k >> 2) * 16384 + (k & 3) * 32;
-                    mma_bf16_ss(tmem + 128, sdesc_sw128(ka + o, 16, 1024), sdesc_sw128(ra + k * 2048, 16384, 1024),
-                                ID_KM, k > 0);
-                }
-                mma_commit(b_inter);
-            }
-            for (int n = 0; n < G && ok; ++n) {
-                const int b = n & 1;
-                ok = mbar_wait(b_qf(b), (n >> 1) & 1, status, 103);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t q_s = qa(b), do_s = da(b);
-#pragma unroll
-                for (int k = 0; k < kD / 16; ++k) {   // S^T = K Q^T
-                    const uint32_t o = (k >> 2) * 16384 + (k & 3) * 32;
-                    mma_bf16_ss(tmem + 256, sdesc_sw128(ka + o, 16, 1024), sdesc_sw128(q_s + o, 16, 1024), ID_KK,
-                                k > 0);
-                }
-#pragma unroll
-                for (int k = 0; k < kD / 16; ++k) {   // A^T = V dO^T
-                    const uint32_t o = (k >> 2) * 16384 + (k & 3) * 32;
-                    mma_bf16_ss(tmem + 384, sdesc_sw128(va + o, 16, 1024), sdesc_sw128(do_s + o, 16, 1024), ID_KK,
-                                k > 0);
-                }
-                mma_commit(b_sa);
-                for (int h = 0; h < 2 && ok; ++h) {
-                    ok = mbar_wait(b_pa(h), n & 1, status, 104);
-                    if (ok && n == 0 && h == 0) ok = mbar_wait(b_scaled, 0, status, 105);   // carried-in rows scaled
+            bool ok = true;
+            for (int i = 0; i < n_items && ok; ++i) {
+                for (int n = 0; n < G && ok; ++n) {
+                    const int u = i * G + n, b = u & 1;
+                    if (n == 0) ok = mbar_wait(b_kv, i & 1, status, 101);   // this chunk's K, V, Rsum
+                    if (ok) ok = mbar_wait(b_qf(b), (u >> 1) & 1, status, 103);
                     if (!ok) break;
                     tc_fence_after();
+                    const uint32_t q_s = qa(b), do_s = da(b);
 #pragma unroll
-                    for (int k = 4 * h; k < 4 * h + 4; ++k)   // dV += P^T dO (queries 16k .. 16k + 15,
-                        mma_bf16_ts(tmem + 128, tmem + 256 + h * 64 + (k & 3) * 8,   // packed at 64h + 8 (k % 4))
-                                    sdesc_sw128(do_s + k * 2048, 16384, 1024), ID_KM, 1u);
+                    for (int k = 0; k < kD / 16; ++k) {   // S^T = K Q^T
+                        const uint32_t o = (k >> 2) * 16384 + (k & 3) * 32;
+                        mma_bf16_ss(tmem + 256, sdesc_sw128(ka + o, 16, 1024), sdesc_sw128(q_s + o, 16, 1024),
+                                    ID_KK, k > 0);
+                    }
 #pragma unroll
-                    for (int k = 4 * h; k < 4 * h + 4; ++k)   // dK += dA^T Q
-                        mma_bf16_ts(tmem, tmem + 384 + h * 64 + (k & 3) * 8, sdesc_sw128(q_s + k * 2048, 16384, 1024),
-                                    ID_KM, 1u);
+                    for (int k = 0; k < kD / 16; ++k) {   // A^T = V dO^T
+                        const uint32_t o = (k >> 2) * 16384 + (k & 3) * 32;
+                        mma_bf16_ss(tmem + 384, sdesc_sw128(va + o, 16, 1024), sdesc_sw128(do_s + o, 16, 1024),
+                                    ID_KK, k > 0);
+                    }
+                    mma_commit(b_sa);
+                    if (n == 0) {
+                        // carried-in parts: dK = V Rsum^T (Rsum rows = key features, i.e.
+                        // K-major for this product), dV = K Rsum (the same tile read
+                        // MN-major), over TMEM the previous chunk's dK, dV have left
+                        if (i > 0) ok = mbar_wait(b_dkvfree, (i - 1) & 1, status, 102);
+                        if (!ok) break;
+                        tc_fence_after();
+#pragma unroll
+                        for (int k = 0; k < kD / 16; ++k) {
+                            const uint32_t o = (k >> 2) * 16384 + (k & 3) * 32;
+                            mma_bf16_ss(tmem, sdesc_sw128(va + o, 16, 1024), sdesc_sw128(ra + o, 16, 1024), ID_KK,
+                                        k > 0);
+                        }
+#pragma unroll
+                        for (int k = 0; k < kD / 16; ++k) {
+                            const uint32_t o = (k >> 2) * 16384 + (k & 3) * 32;
+                            mma_bf16_ss(tmem + 128, sdesc_sw128(ka + o, 16, 1024),
+                                        sdesc_sw128(ra + k * 2048, 16384, 1024), ID_KM, k > 0);
+                        }
+                        mma_commit(b_inter);
+                    }
+                    if (n == G - 1) mma_commit(b_kvfree);   // K, V, Rsum read by the chunk's last products
+                    for (int h = 0; h < 2 && ok; ++h) {
+                        ok = mbar_wait(b_pa(h), u & 1, status, 104);
+                        if (ok && n == 0 && h == 0) ok = mbar_wait(b_scaled, i & 1, status, 105);   // carried-in scaled
+                        if (!ok) break;
+                        tc_fence_after();
+#pragma unroll
+                        for (int k = 4 * h; k < 4 * h + 4; ++k)   // dV += P^T dO (queries 16k .. 16k + 15,
+                            mma_bf16_ts(tmem + 128, tmem + 256 + h * 64 + (k & 3) * 8,   // packed at 64h + 8 (k % 4))
+                                        sdesc_sw128(do_s + k * 2048, 16384, 1024), ID_KM, 1u);
+#pragma unroll
+                        for (int k = 4 * h; k < 4 * h + 4; ++k)   // dK += dA^T Q
+                            mma_bf16_ts(tmem, tmem + 384 + h * 64 + (k & 3) * 8,
+                                        sdesc_sw128(q_s + k * 2048, 16384, 1024), ID_KM, 1u);
+                    }
+                    if (!ok) break;
+                    mma_commit(b_qe(b));   // slot b free again once these products have read it
                 }
-                if (!ok) break;
-                mma_commit(b_qe(b));   // slot b free again once these products have read it
+                if (ok) mma_commit(b_done);   // this chunk's dK, dV complete
             }
-            if (ok) mma_commit(b_done);
             mma_commit(b_drain);
             mbar_wait(b_drain, 0, status, 106);
         }
@@ -890,79 +912,86 @@ __global__ void __launch_bounds__(kLinThreads, 1)
         const int hc = warp >> 2;                  // query half; dK (0) or dV (1)
         const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) << 5) << 16);
         const float lg = log2f(decay[g]);
-        bool ok = mbar_wait(b_inter, 0, status, 107);
-        ok = __all_sync(0xffffffffu, ok);
-        if (ok) {
-            // carried-in rows weigh gamma^(L-1-m') (0 past the chunk)
-            tc_fence_after();
-            const float w = m < L ? exp2f((float)(L - 1 - m) * lg) : 0.f;
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {   // dK (half 0) or dV (half 1)
-                float v[32];
-                tmem_ld32(lane_base + hc * 128 + cc * 32, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int u = 0; u < 32; ++u) v[u] *= w;
-                tmem_st32(lane_base + hc * 128 + cc * 32, v);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(b_scaled);
-        }
         const float* wt = wtab + 128 - m;   // wt[m] = scale * gamma^(m - m'), 0 for m < m'
-        for (int n = 0; n < G; ++n) {
-            if (ok) ok = mbar_wait(b_sa, n & 1, status, 108);
+        bool ok = true;
+        for (int i = 0; i < n_items; ++i) {
+            const int chunk = chunk_of(i), off = chunks[4 * chunk], L = chunks[4 * chunk + 1];
+            if (ok) ok = mbar_wait(b_inter, i & 1, status, 107);
             ok = __all_sync(0xffffffffu, ok);
-            if (!ok) continue;
-            tc_fence_after();
-            // P^T[m', m] = scale S^T gamma^(m-m'), dA^T[m', m] = scale A^T gamma^(m-m'),
-            // for m' <= m < L; this half's 64 queries packed as bf16 over the first
-            // 32 of its columns in each region
-#pragma unroll 2
-            for (int cq = 0; cq < 4; ++cq) {   // 16 columns at a time
-                const int cc = 4 * hc + cq;
-                float s[16], a[16];
-                tmem_ld16(lane_base + 256 + cc * 16, s);
-                tmem_ld16(lane_base + 384 + cc * 16, a);
-                tmem_wait_ld();
-                uint32_t pw[8], aw[8];
+            if (ok) {
+                // carried-in rows weigh gamma^(L-1-m') (0 past the chunk)
+                tc_fence_after();
+                const float w = m < L ? exp2f((float)(L - 1 - m) * lg) : 0.f;
 #pragma unroll
-                for (int w2 = 0; w2 < 8; ++w2) {
-                    const int c0 = cc * 16 + 2 * w2, c1 = c0 + 1;
-                    const float w0 = c0 < L ? wt[c0] : 0.f;
-                    const float w1 = c1 < L ? wt[c1] : 0.f;
-                    pw[w2] = pack_bf16x2(s[2 * w2] * w0, s[2 * w2 + 1] * w1);
-                    aw[w2] = pack_bf16x2(a[2 * w2] * w0, a[2 * w2 + 1] * w1);
+                for (int cc = 0; cc < 4; ++cc) {   // dK (half 0) or dV (half 1)
+                    float v[32];
+                    tmem_ld32(lane_base + hc * 128 + cc * 32, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) v[x] *= w;
+                    tmem_st32(lane_base + hc * 128 + cc * 32, v);
                 }
-                // over columns this thread has already read
-                tmem_st8(lane_base + 256 + hc * 64 + cq * 8, pw);
-                tmem_st8(lane_base + 384 + hc * 64 + cq * 8, aw);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(b_scaled);
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(b_pa(hc));
-        }
-        if (ok) ok = mbar_wait(b_done, 0, status, 109);
-        ok = __all_sync(0xffffffffu, ok);
-        if (ok) {
-            tc_fence_after();
-            uint4* dst = reinterpret_cast<uint4*>((hc ? dv : dk) + ((size_t)(off + m) * hkv + g) * kD);
+            for (int n = 0; n < G; ++n) {
+                const int u = i * G + n;
+                if (ok) ok = mbar_wait(b_sa, u & 1, status, 108);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) continue;
+                tc_fence_after();
+                // P^T[m', m] = scale S^T gamma^(m-m'), dA^T[m', m] = scale A^T gamma^(m-m'),
+                // for m' <= m < L; this half's 64 queries packed as bf16 over the first
+                // 32 of its columns in each region
+#pragma unroll 2
+                for (int cq = 0; cq < 4; ++cq) {   // 16 columns at a time
+                    const int cc = 4 * hc + cq;
+                    float s[16], a[16];
+                    tmem_ld16(lane_base + 256 + cc * 16, s);
+                    tmem_ld16(lane_base + 384 + cc * 16, a);
+                    tmem_wait_ld();
+                    uint32_t pw[8], aw[8];
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                float v[32];
-                tmem_ld32(lane_base + hc * 128 + cc * 32, v);
-                tmem_wait_ld();
-                if (m < L) {
+                    for (int w2 = 0; w2 < 8; ++w2) {
+                        const int c0 = cc * 16 + 2 * w2, c1 = c0 + 1;
+                        const float w0 = c0 < L ? wt[c0] : 0.f;
+                        const float w1 = c1 < L ? wt[c1] : 0.f;
+                        pw[w2] = pack_bf16x2(s[2 * w2] * w0, s[2 * w2 + 1] * w1);
+                        aw[w2] = pack_bf16x2(a[2 * w2] * w0, a[2 * w2 + 1] * w1);
+                    }
+                    // over columns this thread has already read
+                    tmem_st8(lane_base + 256 + hc * 64 + cq * 8, pw);
+                    tmem_st8(lane_base + 384 + hc * 64 + cq * 8, aw);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(b_pa(hc));
+            }
+            if (ok) ok = mbar_wait(b_done, i & 1, status, 109);
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok) {
+                tc_fence_after();
+                uint4* dst = reinterpret_cast<uint4*>((hc ? dv : dk) + ((size_t)(off + m) * hkv + g) * kD);
 #pragma unroll
-                    for (int w = 0; w < 4; ++w) {
-                        uint4 x;
-                        x.x = pack_bf16x2(v[8 * w], v[8 * w + 1]);
-                        x.y = pack_bf16x2(v[8 * w + 2], v[8 * w + 3]);
-                        x.z = pack_bf16x2(v[8 * w + 4], v[8 * w + 5]);
-                        x.w = pack_bf16x2(v[8 * w + 6], v[8 * w + 7]);
-                        dst[cc * 4 + w] = x;
+                for (int cc = 0; cc < 4; ++cc) {
+                    float v[32];
+                    tmem_ld32(lane_base + hc * 128 + cc * 32, v);
+                    tmem_wait_ld();
+                    if (m < L) {
+#pragma unroll
+                        for (int x = 0; x < 4; ++x) {
+                            uint4 y;
+                            y.x = pack_bf16x2(v[8 * x], v[8 * x + 1]);
+                            y.y = pack_bf16x2(v[8 * x + 2], v[8 * x + 3]);
+                            y.z = pack_bf16x2(v[8 * x + 4], v[8 * x + 5]);
+                            y.w = pack_bf16x2(v[8 * x + 6], v[8 * x + 7]);
+                            dst[cc * 4 + x] = y;
+                        }
                     }
                 }
+                tc_fence_before();
+                mbar_arrive(b_dkvfree);   // TMEM dK, dV may take the next chunk's carried-in parts
             }
         }
     }
@@ -1105,7 +1134,8 @@ int tree_attn_linear_bwd(tree_attn_plan_t P, const void* q, const void* k, const
     lin_bwd_scan_kernel<<<dim3(kD * kD / 256, hkv), 256, 0, s>>>(D->lnodes, P->n_nodes, (int)nc, D->chunks, decay, hkv, r0, r1,
                                                                  r2);
     if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
-    lin_bwd_kv_kernel<<<(unsigned)(nc * hkv), kLinThreads, kKvSmem, s>>>(tq, tk, tv, tdo, tr1, D->chunks, decay,
+    lin_bwd_kv_kernel<<<(unsigned)(lanes * hkv), kLinThreads, kKvSmem, s>>>(tq, tk, tv, tdo, tr1, D->chunks, (int)nc,
+                                                                         lanes, decay,
                                                                  static_cast<uint16_t*>(dk), static_cast<uint16_t*>(dv),
                                                                  hq, hkv, scale, status);
     return cudaGetLastError() == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;

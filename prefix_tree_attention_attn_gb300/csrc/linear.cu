@@ -515,6 +515,15 @@ int build_lin(tree_attn_plan_s* P) {
             X.lnodes[4 * (size_t)k + 1] = first;
             X.lnodes[4 * (size_t)k + 2] = nc - first;
         }
+        // fourth field: 1 for the last child of its parent in packed order (the
+        // first one the reverse scan leaves), else 0
+        std::vector<int32_t> last_child(n, -1);
+        for (int32_t k = 0; k < n; ++k) {
+            const int32_t pp = X.lnodes[4 * (size_t)k];
+            if (pp >= 0) last_child[pp] = k;   // children in increasing packed position
+        }
+        for (int32_t k = 0; k < n; ++k)
+            if (last_child[k] >= 0) X.lnodes[4 * (size_t)last_child[k] + 3] = 1;
         X.ready = true;
     } catch (const std::bad_alloc&) {
         return TREE_ATTN_ERR_OUT_OF_MEMORY;
@@ -684,55 +693,85 @@ __global__ void __launch_bounds__(160, 1)
 }
 
 // ---- adjoints, chunk by chunk in reverse packed order ------------------------
-// One thread per (state entry, kv-head).  A node's children come after it in
-// packed order, so walking the chunks backwards every child's entering adjoint
-// has been added into its parent's slot (csum) before the parent's last chunk
-// is reached.  kBwdScanBatch adjoint increments are loaded at a time, as in the
-// forward scan (a smaller batch here measured faster than the forward's).  The
-// sums run in fp32; Rsum leaves as bf16, the dK/dV kernel's operand precision.
-constexpr int kBwdScanBatch = 8;
+// One thread per (state entry, kv-head).  Walking the chunks backwards, a node
+// is left (its first chunk done) with its entering adjoint, which adds into its
+// parent's sum of children; the parent is entered (its last chunk reached)
+// right after its first child is left, since the first child follows its parent
+// in packed order.  The running sum of the parent whose children are being left
+// stays in a register (`pend`, for node `ppar`): a child of another parent
+// stores it to `csum` and starts that parent's sum -- from 0 for its last child,
+// the first one met, else from the partial sum stored earlier -- and entering a
+// node with children takes `pend` as its entering sum.  The additions run in
+// the same order as one read-modify-write per child would.  kBwdScanBatch
+// increments are loaded at a time, as in the forward scan; the sums run in fp32
+// and Rsum leaves as bf16, the dK/dV kernel's operand precision.
+constexpr int kBwdScanBatch = 16;
 
-__global__ void __launch_bounds__(256) lin_bwd_scan_kernel(const int32_t* __restrict__ lnodes, int n_nodes,
-                                                         int n_chunks, const int32_t* __restrict__ chunks,
+__global__ void __launch_bounds__(256) lin_bwd_scan_kernel(const int32_t* __restrict__ lnodes, int n_chunks,
+                                                         const int32_t* __restrict__ chunks,
                                                          const float* __restrict__ decay, int hkv,
                                                          const float* __restrict__ f_in, uint16_t* __restrict__ rsum16,
                                                          float* __restrict__ csum) {
+    __shared__ float w_fac[kScanWin];
+    __shared__ int w_node[kScanWin], w_par[kScanWin], w_last[kScanWin];
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
     const int g = blockIdx.y;
     const size_t dd = (size_t)kD * kD;
     const float lg = log2f(decay[g]);
-    for (int k = 0; k < n_nodes; ++k) csum[((size_t)k * hkv + g) * dd + e] = 0.f;
-    float acc = 0.f;
-    int cur = -1;   // the node whose chunks are being walked
-    for (int c = n_chunks - 1; c >= 0; c -= kBwdScanBatch) {
-        float fv[kBwdScanBatch];
-        int len[kBwdScanBatch], node[kBwdScanBatch];
+    auto sum_at = [&](int node) { return ((size_t)node * hkv + g) * dd + e; };
+    float acc = 0.f, pend = 0.f;
+    int cur = -1, cur_par = -1, cur_last = 0, ppar = -1;
+    // node `cur` has been walked down to its first chunk: its entering adjoint
+    // `acc` goes to its parent
+    auto leave = [&]() {
+        if (cur < 0 || cur_par < 0) return;
+        if (ppar == cur_par) {
+            pend += acc;
+        } else {
+            if (ppar >= 0) csum[sum_at(ppar)] = pend;
+            pend = cur_last ? acc : csum[sum_at(cur_par)] + acc;
+            ppar = cur_par;
+        }
+    };
+    // windows [w0 - nw, w0) from the end; inside a window, chunk w0 - 1 - t is t
+    for (int w0 = n_chunks; w0 > 0; w0 -= kScanWin) {
+        const int nw = min(kScanWin, w0);
+        __syncthreads();
+        for (int t = threadIdx.x; t < nw; t += blockDim.x) {
+            const int node = chunks[4 * (w0 - 1 - t) + 2];
+            w_fac[t] = exp2f((float)chunks[4 * (w0 - 1 - t) + 1] * lg);
+            w_node[t] = node;
+            w_par[t] = lnodes[4 * node];
+            w_last[t] = lnodes[4 * node + 3];
+        }
+        __syncthreads();
+        for (int c = 0; c < nw; c += kBwdScanBatch) {
+            float fv[kBwdScanBatch];
 #pragma unroll
-        for (int u = 0; u < kBwdScanBatch; ++u)
-            if (c - u >= 0) {
-                fv[u] = f_in[((size_t)(c - u) * hkv + g) * dd + e];
-                len[u] = chunks[4 * (c - u) + 1];
-                node[u] = chunks[4 * (c - u) + 2];
-            }
+            for (int u = 0; u < kBwdScanBatch; ++u)
+                if (c + u < nw) fv[u] = f_in[((size_t)(w0 - 1 - c - u) * hkv + g) * dd + e];
 #pragma unroll
-        for (int u = 0; u < kBwdScanBatch; ++u)
-            if (c - u >= 0) {
-                if (node[u] != cur) {   // last chunk of a node: start from its children's sum
-                    if (cur >= 0) {
-                        const int par = lnodes[4 * cur];
-                        if (par >= 0) csum[((size_t)par * hkv + g) * dd + e] += acc;
+            for (int u = 0; u < kBwdScanBatch; ++u)
+                if (c + u < nw) {
+                    const int node = w_node[c + u];
+                    if (node != cur) {   // last chunk of a node
+                        leave();
+                        cur = node;
+                        cur_par = w_par[c + u];
+                        cur_last = w_last[c + u];
+                        if (ppar == node) {   // its children's sum (none: a leaf, 0)
+                            acc = pend;
+                            ppar = -1;
+                        } else {
+                            acc = 0.f;
+                        }
                     }
-                    cur = node[u];
-                    acc = csum[((size_t)cur * hkv + g) * dd + e];
+                    rsum16[state16_index(w0 - 1 - c - u, e, g, hkv)] = float_to_bf16_bits(acc);
+                    acc = fv[u] + w_fac[c + u] * acc;
                 }
-                rsum16[state16_index(c - u, e, g, hkv)] = float_to_bf16_bits(acc);
-                acc = fv[u] + exp2f((float)len[u] * lg) * acc;
-            }
+        }
     }
-    if (cur >= 0) {
-        const int par = lnodes[4 * cur];
-        if (par >= 0) csum[((size_t)par * hkv + g) * dd + e] += acc;
-    }
+    leave();
 }
 
 // ---- dK, dV per (chunk, kv-head) ------------------------------------------------
@@ -1131,8 +1170,7 @@ int tree_attn_linear_bwd(tree_attn_plan_t P, const void* q, const void* k, const
     // dK, dV: adjoint increments, the reverse scan, then the per-chunk products
     lin_bwd_f_kernel<<<(unsigned)(nc * hkv), 160, kAdjSmem, s>>>(tq, tdo, D->chunks, decay, hq, hkv, scale, r0, status);
     if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
-    lin_bwd_scan_kernel<<<dim3(kD * kD / 256, hkv), 256, 0, s>>>(D->lnodes, P->n_nodes, (int)nc, D->chunks, decay, hkv, r0, r1,
-                                                                 r2);
+    lin_bwd_scan_kernel<<<dim3(kD * kD / 256, hkv), 256, 0, s>>>(D->lnodes, (int)nc, D->chunks, decay, hkv, r0, r1, r2);
     if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
     lin_bwd_kv_kernel<<<(unsigned)(lanes * hkv), kLinThreads, kKvSmem, s>>>(tq, tk, tv, tdo, tr1, D->chunks, (int)nc,
                                                                          lanes, decay,

@@ -36,7 +36,8 @@ struct DevicePlan {
     // chunk tables of the linear-attention calls (uploaded on their first use)
     void* lin_base = nullptr;
     int32_t* chunks = nullptr;     // [4*n_chunks] {first token, tokens, packed node, 0}
-    int32_t* lnodes = nullptr;     // [4*n_nodes] per packed node {parent's packed index, first chunk, chunks, 0}
+    int32_t* lnodes = nullptr;     // [4*n_nodes] per packed node {parent's packed index, first chunk, chunks,
+                                   //   1 if the last child of its parent}
     bool lin_ready = false;
 };
 

@@ -60,18 +60,31 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
     }
 }
 
-// dQ: 4 elements per thread.
+// dQ: kConvertPer groups of 4 elements per thread, a block's groups contiguous
+// (each of the thread's loads is one coalesced row of the block), all loads
+// issued before the first store.
+constexpr int kConvertPer = 4;
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ src, uint16_t* __restrict__ dst,
                                                          int64_t n4) {
     grid_dep_wait();   // the accumulator is complete once the main pass has finished
     grid_dep_launch();
-    const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (k >= n4) return;
-    const float4 v = reinterpret_cast<const float4*>(src)[k];
-    uint2 w;
-    w.x = (uint32_t)float_to_bf16_bits(v.x) | ((uint32_t)float_to_bf16_bits(v.y) << 16);
-    w.y = (uint32_t)float_to_bf16_bits(v.z) | ((uint32_t)float_to_bf16_bits(v.w) << 16);
-    reinterpret_cast<uint2*>(dst)[k] = w;
+    const int64_t base = (int64_t)blockIdx.x * blockDim.x * kConvertPer + threadIdx.x;
+    float4 v[kConvertPer];
+#pragma unroll
+    for (int u = 0; u < kConvertPer; ++u) {
+        const int64_t k = base + (int64_t)u * blockDim.x;
+        if (k < n4) v[u] = reinterpret_cast<const float4*>(src)[k];
+    }
+#pragma unroll
+    for (int u = 0; u < kConvertPer; ++u) {
+        const int64_t k = base + (int64_t)u * blockDim.x;
+        if (k < n4) {
+            uint2 w;
+            w.x = (uint32_t)float_to_bf16_bits(v[u].x) | ((uint32_t)float_to_bf16_bits(v[u].y) << 16);
+            w.y = (uint32_t)float_to_bf16_bits(v[u].z) | ((uint32_t)float_to_bf16_bits(v[u].w) << 16);
+            reinterpret_cast<uint2*>(dst)[k] = w;
+        }
+    }
 }
 
 // One block per (split kv-tile, kv-head, dK|dV, group of 16 rows); thread = 4
@@ -172,7 +185,7 @@ cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t stream) {
 
 cudaError_t launch_bwd_post(const BwdPostParams& p, cudaStream_t stream) {
     const int64_t n4 = (int64_t)p.N * p.hq * p.d / 4;
-    const int64_t blocks = (n4 + 255) / 256;
+    const int64_t blocks = (n4 + 256 * kConvertPer - 1) / (256 * kConvertPer);
     if (blocks > INT32_MAX) return cudaErrorInvalidValue;
     cudaError_t e = cudaSuccess;
     if (blocks > 0) e = launch_pdl(dq_convert_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, p.dq_acc, p.dq, n4);

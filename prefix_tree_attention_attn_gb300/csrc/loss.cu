@@ -36,21 +36,32 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 }
 
 // ---- y = x * w (per row) -------------------------------------------------
-// CTAs stride over rows; the threads of a CTA over a row's 16-byte vectors.
+// The tensor as one run of 16-byte vectors: each thread takes kScalePer of
+// them, a block's vectors contiguous, all loads issued before the first store.
+constexpr int kScalePer = 4;
 __global__ void __launch_bounds__(256) scale_rows_kernel(const uint4* __restrict__ x, const float* __restrict__ w,
-                                                        uint4* __restrict__ y, int64_t n_rows, int64_t vec_per_row) {
-    for (int64_t row = blockIdx.x; row < n_rows; row += gridDim.x) {
-        const float s = w[row];
-        const uint4* xr = x + row * vec_per_row;
-        uint4* yr = y + row * vec_per_row;
-        for (int64_t k = threadIdx.x; k < vec_per_row; k += blockDim.x) {
-            const uint4 a = xr[k];
+                                                        uint4* __restrict__ y, int64_t n_vec, int64_t vec_per_row) {
+    const int64_t base = (int64_t)blockIdx.x * blockDim.x * kScalePer + threadIdx.x;
+    uint4 a[kScalePer];
+    float s[kScalePer];
+#pragma unroll
+    for (int u = 0; u < kScalePer; ++u) {
+        const int64_t k = base + (int64_t)u * blockDim.x;
+        if (k < n_vec) {
+            a[u] = x[k];
+            s[u] = w[k / vec_per_row];
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < kScalePer; ++u) {
+        const int64_t k = base + (int64_t)u * blockDim.x;
+        if (k < n_vec) {
             uint4 b;
-            b.x = pack2(bf16_lo(a.x) * s, bf16_hi(a.x) * s);
-            b.y = pack2(bf16_lo(a.y) * s, bf16_hi(a.y) * s);
-            b.z = pack2(bf16_lo(a.z) * s, bf16_hi(a.z) * s);
-            b.w = pack2(bf16_lo(a.w) * s, bf16_hi(a.w) * s);
-            yr[k] = b;
+            b.x = pack2(bf16_lo(a[u].x) * s[u], bf16_hi(a[u].x) * s[u]);
+            b.y = pack2(bf16_lo(a[u].y) * s[u], bf16_hi(a[u].y) * s[u]);
+            b.z = pack2(bf16_lo(a[u].z) * s[u], bf16_hi(a[u].z) * s[u]);
+            b.w = pack2(bf16_lo(a[u].w) * s[u], bf16_hi(a[u].w) * s[u]);
+            y[k] = b;
         }
     }
 }
@@ -303,9 +314,11 @@ int tree_attn_scale_rows(const void* x, const float* w, void* y, int64_t n_rows,
     int st = current_device(&dev);
     if (st) return st;
     const int64_t vpr = row_elems / 8;
-    const int grid = (int)std::min<int64_t>(n_rows, 152 * 16);
-    scale_rows_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint4*>(x), w, static_cast<uint4*>(y), n_rows, vpr);
+    const int64_t n_vec = n_rows * vpr;
+    const int64_t blocks = (n_vec + 256 * kScalePer - 1) / (256 * kScalePer);
+    if (blocks > INT32_MAX) return TREE_ATTN_ERR_TOO_LARGE;
+    scale_rows_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4*>(x), w, static_cast<uint4*>(y), n_vec, vpr);
     return cudaGetLastError() == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
 }
 

@@ -111,6 +111,18 @@ def test_bwd_random_trees(seed):
     check_bwd(t, 4, 2, [0.97, 1.0], 40 + seed)
 
 
+def test_persistent_kernels_walk_several_chunks():
+    # 16 kv-heads leave 9 chunk lanes on a 152-SM GPU, so each CTA of the output
+    # and dK/dV kernels walks several chunks of ragged lengths (the next chunk's
+    # K, V and state load while the current one runs)
+    t = WT.Tree("wide", [-1] + [0] * 6, [640, 700, 333, 129, 517, 256, 901])
+    nc, _ = linear_workspace(TreePlan(t.parent, t.seg_len), 16, 128)
+    assert nc >= 3 * (torch.cuda.get_device_properties(0).multi_processor_count // 16)
+    decay = [0.97 + 0.002 * i for i in range(16)]
+    check(t, 32, 16, decay, 91)
+    check_bwd(t, 32, 16, decay, 92)
+
+
 @pytest.mark.parametrize("seed", range(2))
 def test_many_nodes(seed):
     # 40 to 60 short nodes: node boundaries at every position of the scans' batches

@@ -142,6 +142,21 @@ def test_backward_cta_orders(order):
     assert np.array_equal(g["dk"], g2["dk"]) and np.array_equal(g["dv"], g2["dv"])
 
 
+def test_d64_persistent_backward_walks_several_units():
+    # 150 tiny binary trees as one forest: 600 (item, kv-head) units for about
+    # one persistent CTA per SM, so every CTA walks several units (second K/V
+    # buffer, steps counted across units, the next unit's first products while
+    # the last one's dK and dV are stored)
+    from prefix_tree_attention_attn_gb300 import batch as TB
+    tiny = WT.load_tree("tiny_binary")
+    fpar, fseg, _ = TB.TreeBatch([(tiny.parent, tiny.seg_len)] * 150).forest([True] * 150)
+    t = WT.Tree("forest", [int(x) for x in fpar], [int(x) for x in fseg])
+    q, k, v, do = draw(t.n_tokens, 4, 2, 64, seed=77)
+    plan, _ = full_parity(t, q, k, v, do, 1 / np.sqrt(64), tag="d64 forest")
+    units = plan.info["n_bwd_items"] * 2
+    assert units >= 2 * torch.cuda.get_device_properties(0).multi_processor_count
+
+
 def test_d64_backward_with_split_items():
     """head_dim 64 with short chunks, so kv-tiles split over several items and
     the fixed-order partial sum runs at d = 64 too."""

@@ -196,6 +196,7 @@ __global__ void __launch_bounds__(160, 1)
 // every thread, are staged in shared memory a window at a time.
 constexpr int kScanBatch = 16;
 constexpr int kScanWin = 1024;
+constexpr int kMaxScanDepths = 32;   // deeper trees use the one-walk scans (one launch per depth otherwise)
 
 __global__ void __launch_bounds__(256) lin_scan_kernel(const int32_t* __restrict__ lnodes, int n_chunks,
                                                      const int32_t* __restrict__ chunks,
@@ -524,6 +525,39 @@ int build_lin(tree_attn_plan_s* P) {
         }
         for (int32_t k = 0; k < n; ++k)
             if (last_child[k] >= 0) X.lnodes[4 * (size_t)last_child[k] + 3] = 1;
+        // children of every node in packed order (CSR), and the nodes grouped by
+        // depth (a parent precedes its children in packed order, so its depth is
+        // known first); depth-by-depth scans only for trees of at most
+        // kMaxScanDepths depths
+        X.kids.assign((size_t)n + 1, 0);
+        for (int32_t k = 0; k < n; ++k)
+            if (X.lnodes[4 * (size_t)k] >= 0) ++X.kids[(size_t)X.lnodes[4 * (size_t)k] + 1];
+        for (int32_t k = 0; k < n; ++k) X.kids[(size_t)k + 1] += X.kids[k];
+        X.kids.resize((size_t)n + 1 + X.kids[n]);
+        {
+            std::vector<int32_t> fill(X.kids.begin(), X.kids.begin() + n);
+            for (int32_t k = 0; k < n; ++k) {
+                const int32_t pp = X.lnodes[4 * (size_t)k];
+                if (pp >= 0) X.kids[(size_t)n + 1 + fill[pp]++] = k;
+            }
+        }
+        std::vector<int32_t> depth(n, 0);
+        int32_t n_depths = 0;
+        for (int32_t k = 0; k < n; ++k) {
+            const int32_t pp = X.lnodes[4 * (size_t)k];
+            depth[k] = pp < 0 ? 0 : depth[pp] + 1;
+            n_depths = std::max(n_depths, depth[k] + 1);
+        }
+        X.lvl_ptr.clear();
+        X.lvl_nodes.clear();
+        if (n_depths <= kMaxScanDepths) {
+            X.lvl_ptr.assign((size_t)n_depths + 1, 0);
+            for (int32_t k = 0; k < n; ++k) ++X.lvl_ptr[(size_t)depth[k] + 1];
+            for (int32_t l = 0; l < n_depths; ++l) X.lvl_ptr[(size_t)l + 1] += X.lvl_ptr[l];
+            X.lvl_nodes.resize(n);
+            std::vector<int32_t> fill(X.lvl_ptr.begin(), X.lvl_ptr.end() - 1);
+            for (int32_t k = 0; k < n; ++k) X.lvl_nodes[fill[depth[k]]++] = k;
+        }
         X.ready = true;
     } catch (const std::bad_alloc&) {
         return TREE_ATTN_ERR_OUT_OF_MEMORY;
@@ -539,10 +573,13 @@ int ensure_lin_device(tree_attn_plan_s* P, DevicePlan** out) {
     if ((st = build_lin(P))) return st;
     DevicePlan& D = P->dev[dev];
     if (!D.lin_ready) {
-        const size_t a = (P->lin.chunks.size() + 63) / 64 * 64, b = P->lin.lnodes.size();
-        std::vector<int32_t> h(a + b, 0);
+        const size_t a = (P->lin.chunks.size() + 63) / 64 * 64, b = P->lin.lnodes.size(),
+                     c = P->lin.lvl_nodes.size(), k = P->lin.kids.size();
+        std::vector<int32_t> h(a + b + c + k, 0);
         std::copy(P->lin.chunks.begin(), P->lin.chunks.end(), h.begin());
         std::copy(P->lin.lnodes.begin(), P->lin.lnodes.end(), h.begin() + a);
+        std::copy(P->lin.lvl_nodes.begin(), P->lin.lvl_nodes.end(), h.begin() + a + b);
+        std::copy(P->lin.kids.begin(), P->lin.kids.end(), h.begin() + a + b + c);
         void* buf = nullptr;
         if (cudaMalloc(&buf, h.size() * sizeof(int32_t)) != cudaSuccess) {
             cudaGetLastError();
@@ -555,6 +592,8 @@ int ensure_lin_device(tree_attn_plan_s* P, DevicePlan** out) {
         D.lin_base = buf;
         D.chunks = static_cast<int32_t*>(buf);
         D.lnodes = static_cast<int32_t*>(buf) + a;
+        D.lvl_nodes = static_cast<int32_t*>(buf) + a + b;
+        D.kids = static_cast<int32_t*>(buf) + a + b + c;
         D.lin_ready = true;
     }
     *out = &D;
@@ -772,6 +811,98 @@ __global__ void __launch_bounds__(256) lin_bwd_scan_kernel(const int32_t* __rest
         }
     }
     leave();
+}
+
+// ---- the same scans, depth by depth ---------------------------------------------
+// For trees of at most kMaxScanDepths depths the scans run one launch per depth
+// (roots first forward, deepest first backward), one thread per (node of that
+// depth, 4 state entries, kv-head): the nodes of a depth are independent, so a
+// thread walks only its own node's chunks instead of every chunk of the tree,
+// four entries at a time (16-byte loads, 8-byte bf16 stores) so that a wide
+// depth needs few waves.  Each entry's arithmetic, and its order, is that of
+// the scans above.
+constexpr int kEntryBlocks = kD * kD / 1024;   // blocks of 256 threads x 4 entries per node
+constexpr int kDepthBatch = 8;
+
+__device__ __forceinline__ uint2 bf16x4(float4 v) {
+    return make_uint2((uint32_t)float_to_bf16_bits(v.x) | ((uint32_t)float_to_bf16_bits(v.y) << 16),
+                      (uint32_t)float_to_bf16_bits(v.z) | ((uint32_t)float_to_bf16_bits(v.w) << 16));
+}
+
+__global__ void __launch_bounds__(256) lin_scan_depth_kernel(const int32_t* __restrict__ lnodes,
+                                                           const int32_t* __restrict__ nodes,
+                                                           const int32_t* __restrict__ chunks,
+                                                           const float* __restrict__ decay, int hkv,
+                                                           const float* __restrict__ ds,
+                                                           uint16_t* __restrict__ s_in16, float* __restrict__ s_out) {
+    const int k = nodes[blockIdx.x / kEntryBlocks];
+    const int e = ((blockIdx.x % kEntryBlocks) * 256 + threadIdx.x) * 4;   // first of 4 state entries
+    const int g = blockIdx.y;
+    const size_t dd = (size_t)kD * kD;
+    const float lg = log2f(decay[g]);
+    const int par = lnodes[4 * k], c0 = lnodes[4 * k + 1], nc = lnodes[4 * k + 2];
+    float4 S = par < 0 ? make_float4(0.f, 0.f, 0.f, 0.f)
+                       : *reinterpret_cast<const float4*>(s_out + ((size_t)par * hkv + g) * dd + e);
+    for (int c = c0; c < c0 + nc; c += kDepthBatch) {
+        float4 dsv[kDepthBatch];
+        int len[kDepthBatch];
+#pragma unroll
+        for (int u = 0; u < kDepthBatch; ++u)
+            if (c + u < c0 + nc) {
+                dsv[u] = *reinterpret_cast<const float4*>(ds + ((size_t)(c + u) * hkv + g) * dd + e);
+                len[u] = chunks[4 * (c + u) + 1];
+            }
+#pragma unroll
+        for (int u = 0; u < kDepthBatch; ++u)
+            if (c + u < c0 + nc) {
+                *reinterpret_cast<uint2*>(s_in16 + state16_index(c + u, e, g, hkv)) = bf16x4(S);
+                const float f = exp2f((float)len[u] * lg);
+                S = make_float4(f * S.x + dsv[u].x, f * S.y + dsv[u].y, f * S.z + dsv[u].z, f * S.w + dsv[u].w);
+            }
+    }
+    *reinterpret_cast<float4*>(s_out + ((size_t)k * hkv + g) * dd + e) = S;
+}
+
+// Backward: a node's entering sum is its children's entering adjoints, added in
+// reverse packed order from 0 (the order of the scan above); its own entering
+// adjoint goes to `ent` for its parent.
+__global__ void __launch_bounds__(256) lin_bwd_scan_depth_kernel(const int32_t* __restrict__ lnodes,
+                                                               const int32_t* __restrict__ kids, int n_nodes,
+                                                               const int32_t* __restrict__ nodes,
+                                                               const int32_t* __restrict__ chunks,
+                                                               const float* __restrict__ decay, int hkv,
+                                                               const float* __restrict__ f_in,
+                                                               uint16_t* __restrict__ rsum16, float* __restrict__ ent) {
+    const int k = nodes[blockIdx.x / kEntryBlocks];
+    const int e = ((blockIdx.x % kEntryBlocks) * 256 + threadIdx.x) * 4;
+    const int g = blockIdx.y;
+    const size_t dd = (size_t)kD * kD;
+    const float lg = log2f(decay[g]);
+    const int c0 = lnodes[4 * k + 1], nc = lnodes[4 * k + 2];
+    const int32_t* kid = kids + n_nodes + 1;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int x = kids[k + 1] - 1; x >= kids[k]; --x) {
+        const float4 a = *reinterpret_cast<const float4*>(ent + ((size_t)kid[x] * hkv + g) * dd + e);
+        acc = make_float4(acc.x + a.x, acc.y + a.y, acc.z + a.z, acc.w + a.w);
+    }
+    for (int c = c0 + nc - 1; c >= c0; c -= kDepthBatch) {
+        float4 fv[kDepthBatch];
+        int len[kDepthBatch];
+#pragma unroll
+        for (int u = 0; u < kDepthBatch; ++u)
+            if (c - u >= c0) {
+                fv[u] = *reinterpret_cast<const float4*>(f_in + ((size_t)(c - u) * hkv + g) * dd + e);
+                len[u] = chunks[4 * (c - u) + 1];
+            }
+#pragma unroll
+        for (int u = 0; u < kDepthBatch; ++u)
+            if (c - u >= c0) {
+                *reinterpret_cast<uint2*>(rsum16 + state16_index(c - u, e, g, hkv)) = bf16x4(acc);
+                const float f = exp2f((float)len[u] * lg);
+                acc = make_float4(fv[u].x + f * acc.x, fv[u].y + f * acc.y, fv[u].z + f * acc.z, fv[u].w + f * acc.w);
+            }
+    }
+    *reinterpret_cast<float4*>(ent + ((size_t)k * hkv + g) * dd + e) = acc;
 }
 
 // ---- dK, dV per (chunk, kv-head) ------------------------------------------------
@@ -1044,6 +1175,45 @@ __global__ void __launch_bounds__(kLinThreads, 1)
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// The forward scan: depth by depth where the plan has the depth tables, else
+// one walk over every chunk.
+int launch_scan(const tree_attn_plan_s* P, const DevicePlan* D, int64_t nc, const float* decay, int hkv,
+                const float* ds, uint16_t* s_in16, float* s_out, cudaStream_t s) {
+    const LinInfo& X = P->lin;
+    if (X.lvl_ptr.empty()) {
+        lin_scan_kernel<<<dim3(kD * kD / 256, hkv), 256, 0, s>>>(D->lnodes, (int)nc, D->chunks, decay, hkv, ds,
+                                                                 s_in16, s_out);
+        return cudaGetLastError() == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
+    }
+    for (size_t l = 0; l + 1 < X.lvl_ptr.size(); ++l) {
+        const int64_t blocks = (int64_t)(X.lvl_ptr[l + 1] - X.lvl_ptr[l]) * kEntryBlocks;
+        if (blocks > INT32_MAX) return TREE_ATTN_ERR_TOO_LARGE;
+        lin_scan_depth_kernel<<<dim3((unsigned)blocks, hkv), 256, 0, s>>>(D->lnodes, D->lvl_nodes + X.lvl_ptr[l],
+                                                                         D->chunks, decay, hkv, ds, s_in16, s_out);
+        if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
+    }
+    return TREE_ATTN_OK;
+}
+
+// The reverse scan: deepest nodes first where the plan has the depth tables.
+int launch_bwd_scan(const tree_attn_plan_s* P, const DevicePlan* D, int64_t nc, const float* decay, int hkv,
+                    const float* f_in, uint16_t* rsum16, float* csum, cudaStream_t s) {
+    const LinInfo& X = P->lin;
+    if (X.lvl_ptr.empty()) {
+        lin_bwd_scan_kernel<<<dim3(kD * kD / 256, hkv), 256, 0, s>>>(D->lnodes, (int)nc, D->chunks, decay, hkv,
+                                                                     f_in, rsum16, csum);
+        return cudaGetLastError() == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
+    }
+    for (size_t l = X.lvl_ptr.size() - 1; l-- > 0;) {
+        const int64_t blocks = (int64_t)(X.lvl_ptr[l + 1] - X.lvl_ptr[l]) * kEntryBlocks;
+        if (blocks > INT32_MAX) return TREE_ATTN_ERR_TOO_LARGE;
+        lin_bwd_scan_depth_kernel<<<dim3((unsigned)blocks, hkv), 256, 0, s>>>(
+            D->lnodes, D->kids, P->n_nodes, D->lvl_nodes + X.lvl_ptr[l], D->chunks, decay, hkv, f_in, rsum16, csum);
+        if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
+    }
+    return TREE_ATTN_OK;
+}
+
 // Chunk lanes of the persistent output kernel: about one CTA per SM in all
 // (lanes x hkv CTAs), at least one lane, at most one per chunk.
 int out_lanes(int dev, int64_t n_chunks, int hkv) {
@@ -1109,9 +1279,7 @@ int tree_attn_linear_fwd(tree_attn_plan_t P, const void* q, const void* k, const
         return TREE_ATTN_ERR_CUDA;
     lin_delta_kernel<<<(unsigned)(nc * hkv), 160, kDeltaSmem, s>>>(tk, tv, D->chunks, decay, hkv, ds, status);
     if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
-    lin_scan_kernel<<<dim3(kD * kD / 256, hkv), 256, 0, s>>>(D->lnodes, (int)nc, D->chunks, decay, hkv, ds, s_in16,
-                                                             s_out);
-    if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
+    if ((st = launch_scan(P, D, nc, decay, hkv, ds, s_in16, s_out, s))) return st;
     const int lanes = out_lanes(dev, nc, hkv);
     lin_out_kernel<<<(unsigned)(lanes * hkv), kLinThreads, kOutSmem, s>>>(tq, tk, tv, ts, D->chunks, (int)nc, lanes,
                                                                       decay, static_cast<uint16_t*>(o), hq, hkv,
@@ -1160,8 +1328,7 @@ int tree_attn_linear_bwd(tree_attn_plan_t P, const void* q, const void* k, const
     // dQ: the forward with (q, k, v) = (dO, V, K)
     lin_delta_kernel<<<(unsigned)(nc * hkv), 160, kDeltaSmem, s>>>(tv, tk, D->chunks, decay, hkv, r0, status);
     if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
-    lin_scan_kernel<<<dim3(kD * kD / 256, hkv), 256, 0, s>>>(D->lnodes, (int)nc, D->chunks, decay, hkv, r0, r1, r2);
-    if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
+    if ((st = launch_scan(P, D, nc, decay, hkv, r0, r1, r2, s))) return st;
     const int lanes = out_lanes(dev, nc, hkv);
     lin_out_kernel<<<(unsigned)(lanes * hkv), kLinThreads, kOutSmem, s>>>(tdo, tv, tk, tr1, D->chunks, (int)nc, lanes,
                                                                       decay, static_cast<uint16_t*>(dq), hq, hkv,
@@ -1170,8 +1337,7 @@ int tree_attn_linear_bwd(tree_attn_plan_t P, const void* q, const void* k, const
     // dK, dV: adjoint increments, the reverse scan, then the per-chunk products
     lin_bwd_f_kernel<<<(unsigned)(nc * hkv), 160, kAdjSmem, s>>>(tq, tdo, D->chunks, decay, hq, hkv, scale, r0, status);
     if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
-    lin_bwd_scan_kernel<<<dim3(kD * kD / 256, hkv), 256, 0, s>>>(D->lnodes, (int)nc, D->chunks, decay, hkv, r0, r1, r2);
-    if (cudaGetLastError() != cudaSuccess) return TREE_ATTN_ERR_CUDA;
+    if ((st = launch_bwd_scan(P, D, nc, decay, hkv, r0, r1, r2, s))) return st;
     lin_bwd_kv_kernel<<<(unsigned)(lanes * hkv), kLinThreads, kKvSmem, s>>>(tq, tk, tv, tdo, tr1, D->chunks, (int)nc,
                                                                          lanes, decay,
                                                                  static_cast<uint16_t*>(dk), static_cast<uint16_t*>(dv),

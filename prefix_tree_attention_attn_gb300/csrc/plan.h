@@ -38,6 +38,8 @@ struct DevicePlan {
     int32_t* chunks = nullptr;     // [4*n_chunks] {first token, tokens, packed node, 0}
     int32_t* lnodes = nullptr;     // [4*n_nodes] per packed node {parent's packed index, first chunk, chunks,
                                    //   1 if the last child of its parent}
+    int32_t* lvl_nodes = nullptr;  // packed nodes by depth (LinInfo::lvl_ptr gives each depth's range)
+    int32_t* kids = nullptr;       // [n_nodes+1] child offsets, then the children in packed order
     bool lin_ready = false;
 };
 
@@ -45,6 +47,9 @@ struct DevicePlan {
 struct LinInfo {
     std::vector<int32_t> chunks;   // as DevicePlan::chunks
     std::vector<int32_t> lnodes;   // as DevicePlan::lnodes
+    std::vector<int32_t> lvl_ptr;  // [depths+1] ranges of lvl_nodes; empty for trees too deep to scan by depth
+    std::vector<int32_t> lvl_nodes;
+    std::vector<int32_t> kids;     // as DevicePlan::kids
     bool ready = false;
 };
 

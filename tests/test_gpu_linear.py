@@ -111,6 +111,14 @@ def test_bwd_random_trees(seed):
     check_bwd(t, 4, 2, [0.97, 1.0], 40 + seed)
 
 
+def test_deep_chain_uses_the_one_walk_scans():
+    # 40 nested nodes: deeper than the depth-by-depth scans take, so both scans
+    # walk every chunk in one pass
+    t = WT.Tree("deep", [-1] + list(range(39)), [(37 * i) % 150 + 1 for i in range(40)])
+    check(t, 4, 2, [0.99, 0.97], 81)
+    check_bwd(t, 4, 2, [0.99, 0.97], 82)
+
+
 def test_persistent_kernels_walk_several_chunks():
     # 16 kv-heads leave 9 chunk lanes on a 152-SM GPU, so each CTA of the output
     # and dK/dV kernels walks several chunks of ragged lengths (the next chunk's

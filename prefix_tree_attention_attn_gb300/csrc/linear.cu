@@ -418,72 +418,86 @@ __global__ void __launch_bounds__(kLinThreads, 1)
         const float fo = scale * exp2f((float)(m + 1) * lg);   // weight of the carried-in part
         const float* wt = mtab + 128 + m;   // wt[-m'] = gamma^(m - m'), 0 past the diagonal
         bool ok = true;
-        for (int u = 0; u < U; ++u) {
-            const int b = u & 1, w = u >> 1, i = u / G, n = u % G, h = g * G + n;
-            const int chunk = chunk_of(i), off = chunks[4 * chunk], L = chunks[4 * chunk + 1];
-            const uint32_t tS = lane_base + 256 * b, tO = tS + 128;
-            if (ok) ok = mbar_wait(b_sf(b), w & 1, status, 86);
-            ok = __all_sync(0xffffffffu, ok);
-            if (ok) {
-                tc_fence_after();
-                // P[m, m'] = scale * S[m, m'] * gamma^(m - m') for m' <= m (rows m >= L
-                // are never stored, and for m < L every m' <= m lies in the chunk)
+        // Unit u's output is stored after unit u+1's mask, so the P V product of
+        // unit u runs while the element-wise warps mask the next unit.
+        int prev_off = 0, prev_L = 0, prev_h = 0;
+        for (int u = 0; u <= U; ++u) {
+            if (u < U) {
+                const int b = u & 1, w = u >> 1;
+                const uint32_t tS = lane_base + 256 * b, tO = tS + 128;
+                if (ok) ok = mbar_wait(b_sf(b), w & 1, status, 86);
+                ok = __all_sync(0xffffffffu, ok);
+                if (ok) {
+                    tc_fence_after();
+                    // P[m, m'] = scale * S[m, m'] * gamma^(m - m') for m' <= m (rows m >= L
+                    // are never stored, and for m < L every m' <= m lies in the chunk)
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    float v[32];
-                    tmem_ld32(tS + col0 + cc * 32, v);
-                    tmem_wait_ld();
-                    uint32_t pw[16];
+                    for (int cc = 0; cc < 2; ++cc) {
+                        float v[32];
+                        tmem_ld32(tS + col0 + cc * 32, v);
+                        tmem_wait_ld();
+                        uint32_t pw[16];
 #pragma unroll
-                    for (int x = 0; x < 16; ++x) {
-                        const int c0 = col0 + cc * 32 + 2 * x, c1 = c0 + 1;
-                        pw[x] = pack_bf16x2(scale * v[2 * x] * wt[-c0], scale * v[2 * x + 1] * wt[-c1]);
+                        for (int x = 0; x < 16; ++x) {
+                            const int c0 = col0 + cc * 32 + 2 * x, c1 = c0 + 1;
+                            pw[x] = pack_bf16x2(scale * v[2 * x] * wt[-c0], scale * v[2 * x + 1] * wt[-c1]);
+                        }
+                        tmem_st16(tS + col0 + cc * 16, pw);
                     }
-                    tmem_st16(tS + col0 + cc * 16, pw);
+                    tmem_wait_st();
+                    ok = mbar_wait(b_o1(b), w & 1, status, 87);
                 }
-                tmem_wait_st();
-                ok = mbar_wait(b_o1(b), w & 1, status, 87);
-            }
-            ok = __all_sync(0xffffffffu, ok);
-            if (ok) {
-                tc_fence_after();
+                ok = __all_sync(0xffffffffu, ok);
+                if (ok) {
+                    tc_fence_after();
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    float v[32];
-                    tmem_ld32(tO + col0 + cc * 32, v);
-                    tmem_wait_ld();
+                    for (int cc = 0; cc < 2; ++cc) {
+                        float v[32];
+                        tmem_ld32(tO + col0 + cc * 32, v);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int x = 0; x < 32; ++x) v[x] *= fo;
-                    tmem_st32(tO + col0 + cc * 32, v);
+                        for (int x = 0; x < 32; ++x) v[x] *= fo;
+                        tmem_st32(tO + col0 + cc * 32, v);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(b_p(b));
                 }
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(b_p(b));
-                ok = mbar_wait(b_o2(b), w & 1, status, 88);
             }
-            ok = __all_sync(0xffffffffu, ok);
-            if (ok) {
-                tc_fence_after();
-                uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)(off + m) * hq + h) * kD + col0);
+            if (u > 0) {   // unit u-1's output
+                const int b = (u - 1) & 1, w = (u - 1) >> 1;
+                const uint32_t tO = lane_base + 256 * b + 128;
+                if (ok) ok = mbar_wait(b_o2(b), w & 1, status, 88);
+                ok = __all_sync(0xffffffffu, ok);
+                if (ok) {
+                    tc_fence_after();
+                    uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)(prev_off + m) * hq + prev_h) * kD + col0);
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    float v[32];
-                    tmem_ld32(tO + col0 + cc * 32, v);
-                    tmem_wait_ld();
-                    if (m < L) {
+                    for (int cc = 0; cc < 2; ++cc) {
+                        float v[32];
+                        tmem_ld32(tO + col0 + cc * 32, v);
+                        tmem_wait_ld();
+                        if (m < prev_L) {
 #pragma unroll
-                        for (int x = 0; x < 4; ++x) {
-                            uint4 y;
-                            y.x = pack_bf16x2(v[8 * x], v[8 * x + 1]);
-                            y.y = pack_bf16x2(v[8 * x + 2], v[8 * x + 3]);
-                            y.z = pack_bf16x2(v[8 * x + 4], v[8 * x + 5]);
-                            y.w = pack_bf16x2(v[8 * x + 6], v[8 * x + 7]);
-                            dst[cc * 4 + x] = y;
+                            for (int x = 0; x < 4; ++x) {
+                                uint4 y;
+                                y.x = pack_bf16x2(v[8 * x], v[8 * x + 1]);
+                                y.y = pack_bf16x2(v[8 * x + 2], v[8 * x + 3]);
+                                y.z = pack_bf16x2(v[8 * x + 4], v[8 * x + 5]);
+                                y.w = pack_bf16x2(v[8 * x + 6], v[8 * x + 7]);
+                                dst[cc * 4 + x] = y;
+                            }
                         }
                     }
+                    tc_fence_before();
+                    mbar_arrive(b_oe(b));   // buffer b may take the unit after next
                 }
-                tc_fence_before();
-                mbar_arrive(b_oe(b));   // buffer b may take the unit after next
+            }
+            if (u < U) {
+                const int chunk = chunk_of(u / G);
+                prev_off = chunks[4 * chunk];
+                prev_L = chunks[4 * chunk + 1];
+                prev_h = g * G + u % G;
             }
         }
     }

@@ -2,22 +2,26 @@
 // recurrent state handed from every node to its children
 // (include/tree_linear.h).
 //
-// Forward, three kernels per call:
+// Forward, three steps per call:
 //   lin_delta_kernel  per (chunk, kv-head): dS = K^T diag(gamma^(L-1-m)) V on
 //                     the tensor core (M = 128 key features, N = 128 value
 //                     features, K = the chunk's tokens), read out of TMEM to
 //                     an fp32 workspace;
-//   lin_scan_kernel   per state entry (d x d x hkv threads): walks the chunks
-//                     in packed order, the entering state of each chunk
+//   the scan          the entering state of each chunk
 //                     S_in = gamma^L S_in(prev) + dS(prev) in fp32, a node's
 //                     first chunk starting from its parent's exit state -- the
 //                     branch-point handoff; S_in leaves as bf16, the operand
-//                     precision of the next kernel;
-//   lin_out_kernel    per (chunk, kv-head), the group's q-heads in turn:
-//                     S = Q K^T, O = Q S_in (S_in TMA-loaded like a value
-//                     tile), then P = S o decay mask (registers, written back
-//                     over S as packed bf16), O rows scaled by gamma^(m+1),
-//                     O += P V; O out as bf16.
+//                     precision of the next kernel.  lin_scan_depth_kernel
+//                     runs one launch per tree depth (each node of that depth,
+//                     4 state entries per thread); trees deeper than
+//                     kMaxScanDepths take lin_scan_kernel, one walk over every
+//                     chunk in packed order per state entry;
+//   lin_out_kernel    persistent, per (chunk, kv-head) and the group's q-heads
+//                     in turn: S = Q K^T, O = Q S_in (S_in TMA-loaded like a
+//                     value tile), then P = S o decay mask (registers, written
+//                     back over S as packed bf16), O rows scaled by
+//                     gamma^(m+1), O += P V; O out as bf16.
+// The backward (below) reuses these for dQ and adds three more for dK, dV.
 #include <cuda_runtime.h>
 
 #include <algorithm>

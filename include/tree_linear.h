@@ -19,9 +19,11 @@
  * Chunked form: every node's segment is cut into chunks of at most 128
  * tokens.  Per chunk and kv-head the state increment
  *   dS_c = sum_{m < L} gamma^(L-1-m) k_m v_m^T               (tensor cores)
- * then, in packed (depth-first) order, the state entering each chunk
+ * then, every node after its parent, the state entering each chunk
  *   S_in(first chunk of u) = S_out(parent(u)),  S_in(next) = gamma^L S_in + dS_c
- * (an elementwise scan, parallel over the d x d state entries), then per chunk
+ * (an elementwise scan in fp32, parallel over the d x d state entries and over
+ * the nodes of one depth; S_in is kept as bf16, the precision the next
+ * products read it in), then per chunk
  * and q-head
  *   O = scale (diag(gamma^(m+1)) Q S_in + ((Q K^T) o D) V),  D[m, m'] = gamma^(m-m') for m' <= m
  * (three tensor-core products, the decay mask in registers).
@@ -31,9 +33,9 @@
  * lives on the device, so the host cannot check it: a value outside (0, 1]
  * (0, negative, above 1, NaN) records TREE_ATTN_ERR_INVALID_DECAY in the
  * device status word (tree_attn_get_device_status) and leaves the call's
- * outputs undefined.  d = 128.  The workspace holds the
- * per-chunk increments and entering states and the per-node exit states
- * (fp32); contents on entry ignored.  Asynchronous on `stream`.
+ * outputs undefined.  d = 128.  The workspace holds the per-chunk increments
+ * (fp32), entering states (bf16) and the per-node exit states (fp32);
+ * contents on entry ignored.  Asynchronous on `stream`.
  */
 #ifndef TREE_LINEAR_H
 #define TREE_LINEAR_H

@@ -23,11 +23,15 @@
 // warps overlap without splitting a step into narrower MMAs.
 //
 // dQ leaves TMEM through the registers of a dedicated readout warpgroup, in
-// two rounds of 64 features through a 32 KB shared staging tile laid out like
-// the fp32 dQ accumulator ([query][feature], 128B-swizzled); an asynchronous
-// TMA reduce-add carries each round to the accumulator.  TMEM is released as
-// soon as the second round's columns are in registers.  With every SM adding
-// 64 KB of dQ per step into L2, this reduce stream is what bounds a step.
+// two rounds of 64 features.  Each round goes out as two 32-feature halves
+// through a 32 KB shared staging tile laid out like the fp32 dQ accumulator
+// ([query][feature], 128B-swizzled, one 16 KB half per 32 features); an
+// asynchronous TMA reduce-add carries each half to the accumulator.  A half is
+// rewritten as soon as the reduce issued two halves earlier has read it, so
+// one reduce is always in flight while the next half is written.  TMEM is
+// released as soon as the second round's columns are in registers.  With every
+// SM adding 64 KB of dQ per step into L2, this reduce stream is what bounds a
+// step.
 //
 // Q tiles go through a 2-slot ring (Q(n) serves S(n), issued during step n-1,
 // and dK(n)); dO tiles through one slot, refilled as soon as dV(n) has read
@@ -62,6 +66,10 @@ __device__ unsigned long long g_bwd_trace[kTrCtas][kTrSteps][kTrEv];
     } while (0)
 #endif
 
+// Wait until every bulk group this thread committed, except the most recent one,
+// has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+
 template <int N>
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[N]) {
     static_assert(N == 16 || N == 32, "columns");
@@ -85,7 +93,7 @@ struct FsCfg {
     static constexpr int OFF_DST = OFF_V + TILE;              // dS^T: 128 keys x 128 queries bf16 (2 blocks)
     static constexpr int OFF_Q = OFF_DST + TILE;              // [2] Q tiles
     static constexpr int OFF_DO = OFF_Q + 2 * TILE;           // dO tile
-    static constexpr int OFF_STAGE = OFF_DO + TILE;           // dQ staging: 128 queries x 64 features fp32
+    static constexpr int OFF_STAGE = OFF_DO + TILE;           // dQ staging: 2 halves of 128 queries x 32 features fp32
     static constexpr int BYTES = OFF_STAGE + 32768;
     static constexpr int NCW = NCW_;                          // compute warps 0 .. NCW-1
     static constexpr int W = 256 / NCW;                       // query columns per compute warp per half-tile
@@ -357,11 +365,12 @@ __global__ void __launch_bounds__(FsCfg<NCW>::NWARPS * 32, 1)
                         if (lane == 0 && warp == C::READOUT0) BWD_TRACE(15, n);
                     }
                 }
-                if (rtid == 0) bulk_wait_read_all();   // the previous reduce has read the tile
-                ok = named_bar_and(2, C::NREADOUT, ok);
-                if (ok) {
 #pragma unroll
-                    for (int blk = 0; blk < 2; ++blk)
+                for (int blk = 0; blk < 2; ++blk) {
+                    // half blk of the staging tile: the reduce issued two halves ago has read it
+                    if (rtid == 0) bulk_wait_read_1();
+                    ok = named_bar_and(2, C::NREADOUT, ok);
+                    if (ok) {
 #pragma unroll
                         for (int k = 0; k < 8; ++k) {
                             const float* s = &v[blk * 32 + 4 * k];
@@ -369,14 +378,14 @@ __global__ void __launch_bounds__(FsCfg<NCW>::NWARPS * 32, 1)
                                          __float_as_uint(s[1] * p.scale), __float_as_uint(s[2] * p.scale),
                                          __float_as_uint(s[3] * p.scale));
                         }
-                }
-                fence_proxy_async_smem();
-                ok = named_bar_and(2, C::NREADOUT, ok);
-                if (ok && rtid == 0) {
-                    for (int blk = 0; blk < 2; ++blk)
+                    }
+                    fence_proxy_async_smem();
+                    ok = named_bar_and(2, C::NREADOUT, ok);
+                    if (ok && rtid == 0) {
                         tma_reduce_add_3d(&tm_dq, stage + blk * 16384, rd * 64 + blk * 32, h, q0);
-                    bulk_commit();
-                    BWD_TRACE(16 + rd, n);
+                        bulk_commit();
+                        BWD_TRACE(16 + rd, n);
+                    }
                 }
             }
         }

@@ -93,9 +93,22 @@ __global__ void __launch_bounds__(FwdCfg<D, NS, PER_SM>::NWARPS * 32, PER_SM)
         return;
     }
 
-    const int n_hg = p.hq / NS;
-    const int t = p.fwd_order[blockIdx.x / n_hg];
-    const int h0 = (blockIdx.x % n_hg) * NS;
+    // CTA order (q-tiles in the planner's order, longest kv-tile list first):
+    // q-tile, then head slice; or, when one q-tile's K/V stream over every kv-head
+    // would crowd L2, kv-head group, then q-tile, then the group's head slices, so
+    // the CTAs running at one time read one kv-head's K/V.
+    int t, h0;
+    if (p.kv_major) {
+        const int per_g = p.group / NS;
+        const int grp = blockIdx.x / (p.T * per_g);
+        const int rem = blockIdx.x - grp * p.T * per_g;
+        t = p.fwd_order[rem / per_g];
+        h0 = grp * p.group + (rem % per_g) * NS;
+    } else {
+        const int n_hg = p.hq / NS;
+        t = p.fwd_order[blockIdx.x / n_hg];
+        h0 = (blockIdx.x % n_hg) * NS;
+    }
     const int hk = h0 / p.group;
     const int q0 = t * 128;
     // debug builds: the q-tile, its kv-tile list and the heads must lie inside

@@ -19,6 +19,7 @@ struct FwdParams {
     int32_t N, hq, group;
     float scale_log2;          // softmax_scale * log2(e)
     int* status;               // device status word
+    int32_t kv_major;          // CTA order: 1 = kv-head group, q-tile, head slice; 0 = q-tile, head slice
     int32_t T;                 // q-tiles (= kv-tiles)          } sizes of the tables,
     int64_t n_ent;             // entries of qt_ent             } for the debug checks
 };

@@ -80,6 +80,37 @@ def test_long_kv_lists(heads):
     full_parity(t, q, k, v, do, 1 / np.sqrt(d), tag=f"long_lists_{hq}_{hkv}")
 
 
+def test_forward_kv_major_order():
+    """A tree whose q-tiles stream more than 64 MB of K and V over all kv-heads
+    (mean kv-tile list x 128 keys x 16 kv-heads x d = 128 x 4 bytes): the
+    forward then takes its CTAs kv-head group by kv-head group.  O and LSE of
+    sampled rows (every head) against the oracle, and every kv-head group run
+    as its own one-kv-head problem (q-tile-major order there) gives the same
+    bits."""
+    from oracle import attention as OA
+    t = WT.Tree("kv_major", [-1] + [0] * 8, [14000] + [600] * 8)
+    plan = TreePlan(t.parent, t.seg_len)
+    hq, hkv, d = 32, 16, 128
+    stream = plan.info["n_tile_entries"] / plan.info["n_qtiles"] * 128 * hkv * d * 4
+    assert stream > 64 * 2**20, stream
+    q, k, v, _ = draw(t.n_tokens, hq, hkv, d, seed=57)
+    scale = 1 / np.sqrt(d)
+    dev = torch.device("cuda:0")
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o, lse = tree_attn_fwd(plan, qd, kd, vd, scale)
+    G = hq // hkv
+    for g in range(hkv):
+        sl = slice(g * G, (g + 1) * G)
+        og, lg = tree_attn_fwd(plan, qd[:, sl].contiguous(), kd[:, g:g + 1].contiguous(),
+                               vd[:, g:g + 1].contiguous(), scale)
+        assert torch.equal(og, o[:, sl]) and torch.equal(lg, lse[sl]), g
+    rows = np.unique(np.concatenate([np.arange(0, t.n_tokens, 997), [127, 128, 14000, 14599, 14600,
+                                                                      t.n_tokens - 1]]))
+    ro, rl = OA.forward_rows(t.parent, t.seg_len, q, k, v, scale, rows)
+    ri = torch.as_tensor(rows, device=dev)
+    assert_fwd(o[ri].float().cpu().numpy(), lse[:, ri].cpu().numpy().astype(np.float64), ro, rl, tag="kv_major")
+
+
 def test_sharp_logits():
     """Unscaled N(0,1) q/k with a large softmax scale: peaked rows, which
     exercise the O rescaling when the running maximum jumps."""

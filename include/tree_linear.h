@@ -26,7 +26,9 @@
  * products read it in), then per chunk
  * and q-head
  *   O = scale (diag(gamma^(m+1)) Q S_in + ((Q K^T) o D) V),  D[m, m'] = gamma^(m-m') for m' <= m
- * (three tensor-core products, the decay mask in registers).
+ * (Q K^T, then one accumulation of the masked scores times V and the scaled
+ * query rows, rounded to bf16, times S_in on the tensor cores; the decay mask
+ * in registers).
  *
  * Tensors as in tree_attn.h: Q, O [N, hq, d] bf16, K, V [N, hkv, d] bf16 in
  * packed order; decay fp32 [hkv] (device), every entry in (0, 1].  The decay

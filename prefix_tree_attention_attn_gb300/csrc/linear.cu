@@ -17,10 +17,11 @@
 //                     kMaxScanDepths take lin_scan_kernel, one walk over every
 //                     chunk in packed order per state entry;
 //   lin_out_kernel    persistent, per (chunk, kv-head) and the group's q-heads
-//                     in turn: S = Q K^T, O = Q S_in (S_in TMA-loaded like a
-//                     value tile), then P = S o decay mask (registers, written
-//                     back over S as packed bf16), O rows scaled by
-//                     gamma^(m+1), O += P V; O out as bf16.
+//                     in turn: S = Q K^T, then P = S o decay mask and the
+//                     query rows scaled by scale * gamma^(m+1) (registers,
+//                     written back over S as packed bf16), O = P V + (f Q) S_in
+//                     in one accumulation (S_in TMA-loaded like a value
+//                     tile); O out as bf16.
 // The backward (below) reuses these for dQ and adds three more for dK, dV.
 #include <cuda_runtime.h>
 
@@ -249,20 +250,25 @@ __global__ void __launch_bounds__(256) lin_scan_kernel(const int32_t* __restrict
 // ---- outputs per (chunk, kv-head): the group's q-heads one after another ------
 // Persistent: a CTA keeps one kv-head g and walks the chunks j0, j0 + lanes,
 // j0 + 2 lanes, ... (grid = lanes x hkv, about one CTA per SM); every
-// (chunk, q-head) pair it meets is one "unit" u.  K, V and the bf16 copy of
-// S_in are loaded once per chunk for the G q-heads of the group; Q comes
-// through two slots and TMEM holds two units (S / P at [256b, 256b + 128), O at
-// [256b + 128, 256b + 256) for buffer b = u & 1), so one unit's P and output
-// overlap the next unit's S and Q S_in products -- across chunk boundaries too:
-// the next chunk's K and S_in load as soon as the last q-head's S and Q S_in
-// products have read them, and its V once the last P V product has read V.
+// (chunk, q-head) pair it meets is one "unit" u.  K is loaded once per chunk,
+// V and the bf16 copy of S_in together once per chunk, for the G q-heads of the
+// group; Q comes through two slots.  TMEM holds two units (buffer b = u & 1):
+// S at [256b, 256b + 128), O at [256b + 128, 256b + 256).
+// Per unit: S = Q K^T; the element-wise warps turn S into the masked P and
+// write, next to it, the query rows scaled by the carried-in weight
+// f(m) = scale * gamma^(m+1), both as packed bf16 (P of keys [64 j, 64 j + 64)
+// at columns [64 j, 64 j + 32), f Q of features [64 j, 64 j + 64) at
+// [64 j + 32, 64 j + 64), over S columns the same threads have read); then one
+// accumulation O = P V + (f Q) S_in of 256 K-steps' worth (A from TMEM).  S of
+// unit u is issued before the products of unit u - 1 (the tensor core runs
+// them in issue order, so P of unit u - 2 in the same buffer has been read),
+// and the products of unit u wait only until unit u - 2's output has left.
 // warps 0-7: query row m = 32 (w % 4) + lane (the TMEM lanes warp w may
 // access), columns [64 (w / 4), 64 (w / 4) + 64) of S and of O -- two warps per
-// row, so that each SM sub-partition has two warps of element-wise work; P of
-// columns [64 j, 64 j + 64) is packed at [64 j, 64 j + 32), over columns the
-// same warps have read.  warp 8: loads; warp 9: TMEM owner, lane 0 issues the
-// MMAs.  The decay mask gamma^(m - m') depends on m - m' alone: its 128 values
-// (and zeros for m' > m) are tabulated once per CTA in shared memory.
+// row, so that each SM sub-partition has two warps of element-wise work.
+// warp 8: loads; warp 9: TMEM owner, lane 0 issues the MMAs.  The decay mask
+// gamma^(m - m') depends on m - m' alone: its 128 values (and zeros for
+// m' > m) are tabulated once per CTA in shared memory.
 constexpr int kOutSmem = 2048 + 5 * kTile;   // barriers, mask table, K, V, S_in (bf16), Q x 2
 constexpr int kLinWarps = 10;                // 8 element-wise warps, loader, MMA issuer
 constexpr int kLinThreads = 32 * kLinWarps;
@@ -285,14 +291,15 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     const int n_items = (n_chunks - 1 - j0) / lanes + 1;   // chunks j0 + i lanes < n_chunks
     const int U = n_items * G;                              // units of this CTA
     auto chunk_of = [&](int i) { return j0 + i * lanes; };
-    // barriers: K and S_in, V, their free signals, then per buffer b: qfull,
-    // qempty, sfull, o1, p, o2, oempty
+    // barriers: K, V with S_in, their free signals, then per buffer b: qfull,
+    // qempty (S has read Q), sfull, qread (the element-wise warps have read Q),
+    // p, o2, oempty
     auto bar = [&](int i) { return sb + 8u * (uint32_t)i; };
-    const uint32_t b_ks = bar(0), b_v = bar(1), b_kfree = bar(18), b_vfree = bar(19);
+    const uint32_t b_k = bar(0), b_v = bar(1), b_kfree = bar(18), b_vfree = bar(19);
     auto b_qf = [&](int b) { return bar(2 + b); };
     auto b_qe = [&](int b) { return bar(4 + b); };
     auto b_sf = [&](int b) { return bar(6 + b); };
-    auto b_o1 = [&](int b) { return bar(8 + b); };
+    auto b_qr = [&](int b) { return bar(8 + b); };
     auto b_p = [&](int b) { return bar(10 + b); };
     auto b_o2 = [&](int b) { return bar(12 + b); };
     auto b_oe = [&](int b) { return bar(14 + b); };
@@ -305,7 +312,7 @@ __global__ void __launch_bounds__(kLinThreads, 1)
         mtab[128 + threadIdx.x] = exp2f((float)threadIdx.x * log2f(decay[g]));
     }
     if (threadIdx.x == 0) {
-        mbar_init(b_ks, 1);
+        mbar_init(b_k, 1);
         mbar_init(b_v, 1);
         mbar_init(b_kfree, 1);
         mbar_init(b_vfree, 1);
@@ -313,7 +320,7 @@ __global__ void __launch_bounds__(kLinThreads, 1)
             mbar_init(b_qf(b), 1);
             mbar_init(b_qe(b), 1);
             mbar_init(b_sf(b), 1);
-            mbar_init(b_o1(b), 1);
+            mbar_init(b_qr(b), 256);
             mbar_init(b_p(b), 256);
             mbar_init(b_o2(b), 1);
             mbar_init(b_oe(b), 256);
@@ -332,29 +339,32 @@ __global__ void __launch_bounds__(kLinThreads, 1)
             bool ok = true;
             for (int i = 0; i < n_items && ok; ++i) {
                 const int chunk = chunk_of(i), off = chunks[4 * chunk];
-                // K and S_in: once the previous chunk's last S and Q S_in products read them
+                // K: once the previous chunk's last S product has read it
                 if (i > 0) ok = mbar_wait(b_kfree, (i - 1) & 1, status, 94);
                 if (!ok) break;
-                mbar_expect_tx(b_ks, 2 * kTile);
-                for (int blk = 0; blk < 2; ++blk) {
-                    tma_load_3d(ka + blk * 16384, &tm_k, blk * 64, g, off, b_ks);
-                    tma_load_3d(sina + blk * 16384, &tm_s, blk * 64, g, chunk * kChunk, b_ks);
-                }
+                mbar_expect_tx(b_k, kTile);
+                for (int blk = 0; blk < 2; ++blk) tma_load_3d(ka + blk * 16384, &tm_k, blk * 64, g, off, b_k);
                 for (int n = 0; n < G && ok; ++n) {
                     const int u = i * G + n, b = u & 1, w = u >> 1;
-                    if (w > 0) ok = mbar_wait(b_qe(b), (w - 1) & 1, status, 89);
+                    if (w > 0) {   // Q slot b: read by unit u - 2's S product and element-wise warps
+                        ok = mbar_wait(b_qe(b), (w - 1) & 1, status, 89);
+                        if (ok) ok = mbar_wait(b_qr(b), (w - 1) & 1, status, 97);
+                    }
                     if (!ok) break;
                     mbar_expect_tx(b_qf(b), kTile);
                     for (int blk = 0; blk < 2; ++blk)
                         tma_load_3d(qa0 + b * kTile + blk * 16384, &tm_q, blk * 64, g * G + n, off, b_qf(b));
-                    // V after the second q-head's Q (the first with one q-head): the
-                    // previous chunk's last P V product, which must have read V, is
+                    // V and S_in after the second q-head's Q (the first with one q-head):
+                    // the previous chunk's last products, which must have read them, are
                     // issued before this chunk's second S product
                     if (n == (G > 1 ? 1 : 0)) {
                         if (i > 0) ok = mbar_wait(b_vfree, (i - 1) & 1, status, 95);
                         if (!ok) break;
-                        mbar_expect_tx(b_v, kTile);
-                        for (int blk = 0; blk < 2; ++blk) tma_load_3d(va + blk * 16384, &tm_v, blk * 64, g, off, b_v);
+                        mbar_expect_tx(b_v, 2 * kTile);
+                        for (int blk = 0; blk < 2; ++blk) {
+                            tma_load_3d(va + blk * 16384, &tm_v, blk * 64, g, off, b_v);
+                            tma_load_3d(sina + blk * 16384, &tm_s, blk * 64, g, chunk * kChunk, b_v);
+                        }
                     }
                 }
             }
@@ -362,25 +372,31 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     } else if (warp == 9) {
         if (lane == 0) {
             constexpr uint32_t ID_S = idesc_bf16(128, 128, false, false);   // Q K^T
-            constexpr uint32_t ID_O = idesc_bf16(128, 128, false, true);    // Q S_in, P V
+            constexpr uint32_t ID_O = idesc_bf16(128, 128, false, true);    // P V, (f Q) S_in
             bool ok = true;
-            auto issue_pv = [&](int u) {
-                const int b = u & 1, i = u / G, n = u % G;
-                if (n == 0) ok = mbar_wait(b_v, i & 1, status, 96);   // this chunk's V
+            auto issue_o = [&](int u) {
+                const int b = u & 1, w = u >> 1, i = u / G, n = u % G;
+                if (w > 0) ok = mbar_wait(b_oe(b), (w - 1) & 1, status, 90);   // unit u - 2's output read
+                if (ok && n == 0) ok = mbar_wait(b_v, i & 1, status, 96);      // this chunk's V and S_in
                 if (!ok) return;
                 tc_fence_after();
+                // keys 16k .. 16k + 15 of P packed at 64 (k / 4) + 8 (k % 4); features
+                // 16k .. 16k + 15 of f Q 32 columns further
 #pragma unroll
-                for (int k = 0; k < kChunk / 16; ++k)   // keys 16k .. 16k + 15 packed at 64 (k / 4) + 8 (k % 4)
+                for (int k = 0; k < kChunk / 16; ++k)
                     mma_bf16_ts(tmem + 256 * b + 128, tmem + 256 * b + (k >> 2) * 64 + (k & 3) * 8,
-                                sdesc_sw128(va + k * 2048, 16384, 1024), ID_O, 1u);
+                                sdesc_sw128(va + k * 2048, 16384, 1024), ID_O, k > 0 ? 1u : 0u);
+#pragma unroll
+                for (int k = 0; k < kD / 16; ++k)
+                    mma_bf16_ts(tmem + 256 * b + 128, tmem + 256 * b + 32 + (k >> 2) * 64 + (k & 3) * 8,
+                                sdesc_sw128(sina + k * 2048, 16384, 1024), ID_O, 1u);
                 mma_commit(b_o2(b));
-                if (n == G - 1) mma_commit(b_vfree);   // V read by the chunk's last P V
+                if (n == G - 1) mma_commit(b_vfree);   // V and S_in read by the chunk's last products
             };
             for (int u = 0; u < U && ok; ++u) {
                 const int b = u & 1, w = u >> 1, i = u / G, n = u % G;
-                if (w > 0) ok = mbar_wait(b_oe(b), (w - 1) & 1, status, 90);   // buffer b read out
-                if (ok) ok = mbar_wait(b_qf(b), w & 1, status, 91);
-                if (ok && n == 0) ok = mbar_wait(b_ks, i & 1, status, 83);   // this chunk's K and S_in
+                ok = mbar_wait(b_qf(b), w & 1, status, 91);
+                if (ok && n == 0) ok = mbar_wait(b_k, i & 1, status, 83);   // this chunk's K
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t qa = qa0 + b * kTile;
@@ -391,24 +407,17 @@ __global__ void __launch_bounds__(kLinThreads, 1)
                                 k > 0);
                 }
                 mma_commit(b_sf(b));
-#pragma unroll
-                for (int k = 0; k < kD / 16; ++k) {
-                    const uint32_t o = (k >> 2) * 16384 + (k & 3) * 32;
-                    mma_bf16_ss(tmem + 256 * b + 128, sdesc_sw128(qa + o, 16, 1024),
-                                sdesc_sw128(sina + k * 2048, 16384, 1024), ID_O, k > 0);
-                }
-                mma_commit(b_o1(b));
-                mma_commit(b_qe(b));                       // Q slot b is no longer read
-                if (n == G - 1) mma_commit(b_kfree);       // K and S_in read by the chunk's last products
-                if (u > 0) {                               // the previous unit's P V
+                mma_commit(b_qe(b));                       // Q slot b no longer read by the tensor core
+                if (n == G - 1) mma_commit(b_kfree);       // K read by the chunk's last S product
+                if (u > 0) {                               // the previous unit's products
                     ok = mbar_wait(b_p((u - 1) & 1), ((u - 1) >> 1) & 1, status, 85);
                     if (!ok) break;
-                    issue_pv(u - 1);
+                    issue_o(u - 1);
                 }
             }
             if (ok) {
                 ok = mbar_wait(b_p((U - 1) & 1), ((U - 1) >> 1) & 1, status, 92);
-                if (ok) issue_pv(U - 1);
+                if (ok) issue_o(U - 1);
             }
             mma_commit(b_drain);
             mbar_wait(b_drain, 0, status, 93);
@@ -416,19 +425,20 @@ __global__ void __launch_bounds__(kLinThreads, 1)
         __syncwarp();
     } else {
         const int m = ((warp & 3) << 5) + lane;   // query row
-        const int col0 = (warp >> 2) * 64;         // this warp's 64 columns of S and of O
+        const int grp = warp >> 2;                 // this warp's 64 columns of S and O, 64 features of Q
+        const int col0 = grp * 64;
         const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) << 5) << 16);
         const float lg = log2f(decay[g]);
         const float fo = scale * exp2f((float)(m + 1) * lg);   // weight of the carried-in part
         const float* wt = mtab + 128 + m;   // wt[-m'] = gamma^(m - m'), 0 past the diagonal
         bool ok = true;
-        // Unit u's output is stored after unit u+1's mask, so the P V product of
-        // unit u runs while the element-wise warps mask the next unit.
+        // Unit u's output is stored after unit u+1's mask, so the products of
+        // unit u run while the element-wise warps mask the next unit.
         int prev_off = 0, prev_L = 0, prev_h = 0;
         for (int u = 0; u <= U; ++u) {
             if (u < U) {
                 const int b = u & 1, w = u >> 1;
-                const uint32_t tS = lane_base + 256 * b, tO = tS + 128;
+                const uint32_t tS = lane_base + 256 * b;
                 if (ok) ok = mbar_wait(b_sf(b), w & 1, status, 86);
                 ok = __all_sync(0xffffffffu, ok);
                 if (ok) {
@@ -448,21 +458,25 @@ __global__ void __launch_bounds__(kLinThreads, 1)
                         }
                         tmem_st16(tS + col0 + cc * 16, pw);
                     }
-                    tmem_wait_st();
-                    ok = mbar_wait(b_o1(b), w & 1, status, 87);
-                }
-                ok = __all_sync(0xffffffffu, ok);
-                if (ok) {
-                    tc_fence_after();
+                    // f(m) q_m over features [col0, col0 + 64), from the 128B-swizzled Q
+                    // slot (block grp holds those features, row m at 128 m)
+                    const uint8_t* qrow = smem + (qa0 - sb) + b * kTile + grp * 16384 + m * 128;
 #pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        float v[32];
-                        tmem_ld32(tO + col0 + cc * 32, v);
-                        tmem_wait_ld();
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        uint32_t qw[16];
 #pragma unroll
-                        for (int x = 0; x < 32; ++x) v[x] *= fo;
-                        tmem_st32(tO + col0 + cc * 32, v);
+                        for (int c = 0; c < 4; ++c) {
+                            const int ch = h2 * 4 + c;   // 16-byte chunk: features 8 ch .. 8 ch + 7
+                            const uint4 x = *reinterpret_cast<const uint4*>(qrow + ((ch ^ (m & 7)) << 4));
+                            const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                qw[4 * c + e] = pack_bf16x2(fo * __uint_as_float(xs[e] << 16),
+                                                            fo * __uint_as_float(xs[e] & 0xffff0000u));
+                        }
+                        tmem_st16(tS + col0 + 32 + h2 * 16, qw);
                     }
+                    mbar_arrive(b_qr(b));   // Q slot b read (the values are in registers)
                     tmem_wait_st();
                     tc_fence_before();
                     mbar_arrive(b_p(b));
@@ -494,7 +508,7 @@ __global__ void __launch_bounds__(kLinThreads, 1)
                         }
                     }
                     tc_fence_before();
-                    mbar_arrive(b_oe(b));   // buffer b may take the unit after next
+                    mbar_arrive(b_oe(b));   // buffer b's O may take the unit after next
                 }
             }
             if (u < U) {
